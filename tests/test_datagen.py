@@ -1,0 +1,61 @@
+"""Seeded generator: determinism, prefix property, structure, format rounding."""
+import numpy as np
+import pytest
+
+from indexer_topk_long_gb300 import datagen
+import oracle.indexer_topk as orc
+
+
+def test_keys_are_prefix_stable_and_deterministic():
+    a = datagen.keys_fp32(20000, 16, seed=1)
+    b = datagen.keys_fp32(9000, 16, seed=1)
+    np.testing.assert_array_equal(a[:9000], b)
+    np.testing.assert_array_equal(a, datagen.keys_fp32(20000, 16, seed=1))
+    assert not np.array_equal(a, datagen.keys_fp32(20000, 16, seed=2))
+
+
+def test_hot_fraction_and_topic_alignment():
+    d = 128
+    k = datagen.keys_fp32(datagen.SEGMENT * 2, d, seed=4)
+    u = datagen.topic_vector(4, 0, d)
+    # hot keys of segment 0 carry +3 along u_0: P(3 + N(0,1) > 4) ~ 16% of ~82 keys;
+    # bulk keys (and segment 1) exceed 4 with probability ~3e-5.
+    own = int(((k[: datagen.SEGMENT] @ u) > 4.0).sum())
+    other = int(((k[datagen.SEGMENT:] @ u) > 4.0).sum())
+    assert own >= 5 and other <= 3
+
+
+def test_query_topic_and_weights():
+    pos = np.arange(8160, 8192, dtype=np.int32)
+    q = datagen.queries_fp32(pos, 8, 128, seed=3)
+    u = datagen.topic_vector(3, 0, 128)
+    assert abs(float((q @ u).mean()) - 1.5) < 0.1
+    w = datagen.weights_fp32(32, 8, seed=3)
+    assert w.min() >= 0 and w.max() < 0.125
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(0).standard_normal(10000).astype(np.float32) * 100
+    ours = datagen.bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ours, ref)
+
+
+def test_e4m3_rounding_is_nearest():
+    x = np.random.default_rng(1).uniform(-448, 448, 20000)
+    codes = datagen.e4m3_codes(x)
+    vals = orc.e4m3_to_f64(codes)
+    grid = orc.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    grid = grid[np.isfinite(grid)]
+    best = np.abs(x[:, None] - grid[None, :]).min(axis=1)
+    np.testing.assert_allclose(np.abs(x - vals), best, rtol=0, atol=1e-12)
+
+
+def test_integer_mode_values():
+    inp = datagen.make_indexer_inputs(T=4, first_pos=100, S=128, H=8, d=16, integer=True, seed=5)
+    q = orc.bf16_to_f64(inp.q)
+    k = orc.bf16_to_f64(inp.k)
+    assert np.all(q == np.round(q)) and np.abs(q).max() <= 3
+    assert np.all(k == np.round(k)) and np.abs(k).max() <= 3
+    assert set(np.unique(inp.w).tolist()) <= {0.5, 0.25, 0.125, 0.0625}
