@@ -1,0 +1,390 @@
+// k_sample.cu -- the Sample stage (LiteTopK technical summary, Methodology
+// step 1 "Sampling (Initialization)").
+//
+// The summary's Sample stage scores a small set of keys -- the top-k' tokens of
+// the previous chunk's results, k' = 3k, instead of a random sample -- to
+// estimate each query's score range [s_min, s_max], splits that range into
+// equal-width bins, and starts the threshold at the bin holding the sample's
+// k-th largest score.  This file provides:
+//   * random_sample    -- seeded stratified sample for a first chunk;
+//   * make_sample      -- previous-chunk sample: key ids ranked by how many of
+//                         the previous chunk's queries selected them;
+//   * prepare_sample   -- drops out-of-range and duplicate ids (a duplicate
+//                         would count one key twice in the sample's k-th score
+//                         and could lift the threshold above the true one);
+//   * gather_keys      -- copies the sample's key rows into a dense tile;
+//   * sample_stats     -- per query: s_min, s_max, delta and the initial
+//                         threshold bin from the scored sample.
+// The sample's scores themselves come from the tensor-core scorer in dense
+// mode over the gathered rows, i.e. the same arithmetic as the Filter scan.
+#include <climits>
+#include <cmath>
+
+#include "ltk_internal.cuh"
+
+namespace ltk {
+namespace {
+
+// SplitMix64 finaliser (Steele, Lea, Flood, "Fast splittable pseudorandom
+// number generators", OOPSLA 2014): a counter-based 64-bit mixer.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  x += 0x9E3779B97F4A7C15ull;
+  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+  return x ^ (x >> 31);
+}
+
+// Bijection of [0, 2^31): xor with a seed, odd multiply mod 2^31, xorshift.
+__device__ __forceinline__ uint32_t perm31(uint32_t x, uint64_t seed) {
+  x ^= static_cast<uint32_t>(seed) & 0x7FFFFFFFu;
+  x = (x * 0x2545F491u) & 0x7FFFFFFFu;
+  x ^= x >> 15;
+  x = (x * 0x6C8E9CF5u) & 0x7FFFFFFFu;
+  x ^= x >> 13;
+  return x;
+}
+
+// One id per stratum [floor(i*S/n), floor((i+1)*S/n)): distinct by
+// construction and spread over the whole cache.
+__global__ void random_sample_kernel(long long S, int n, unsigned long long seed, int* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const long long lo = static_cast<long long>(i) * S / n;
+  const long long hi = static_cast<long long>(i + 1) * S / n;
+  const long long span = hi - lo;
+  const uint64_t r = splitmix64(seed ^ (0xD1B54A32D192ED03ull * static_cast<uint64_t>(i + 1)));
+  out[i] = static_cast<int>(lo + (span > 0 ? static_cast<long long>(r % static_cast<uint64_t>(span)) : 0));
+}
+
+constexpr int kPrepThreads = 1024;
+
+// Sort the ids, keep the first copy of each valid id; the padded tail and
+// dropped ids get INT_MAX ("no key").
+__global__ void __launch_bounds__(kPrepThreads) prepare_sample_kernel(const int* ids, int n,
+                                                                      long long S, int n_pad,
+                                                                      int* key_ids_pad) {
+  extern __shared__ int sid[];
+  int P = 1;
+  while (P < n) P <<= 1;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    int v = INT_MAX;
+    if (i < n) {
+      const int x = ids[i];
+      if (x >= 0 && static_cast<long long>(x) < S) v = x;
+    }
+    sid[i] = v;
+  }
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const int a = sid[lo], b = sid[hi];
+        if ((a > b) == up) {
+          sid[lo] = b;
+          sid[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int r = threadIdx.x; r < n_pad; r += blockDim.x) {
+    int v = INT_MAX;
+    if (r < n) {
+      const int x = sid[r];
+      if (x != INT_MAX && (r == 0 || sid[r - 1] != x)) v = x;
+    }
+    key_ids_pad[r] = v;
+  }
+}
+
+// Copy sample rows (16-byte vectors); missing ids give zero rows.
+__global__ void gather_keys_kernel(const uint4* __restrict__ k_cache, const float* __restrict__ k_scale,
+                                   int vec_per_row, const int* __restrict__ key_ids_pad, int n_pad,
+                                   uint4* __restrict__ k_samp, float* __restrict__ k_scale_samp) {
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(n_pad) * vec_per_row;
+  if (gid >= total) return;
+  const int r = static_cast<int>(gid / vec_per_row);
+  const int v = static_cast<int>(gid % vec_per_row);
+  const int id = key_ids_pad[r];
+  uint4 x = make_uint4(0, 0, 0, 0);
+  if (id != INT_MAX) x = k_cache[static_cast<long long>(id) * vec_per_row + v];
+  k_samp[gid] = x;
+  if (k_scale != nullptr && v == 0) k_scale_samp[r] = (id != INT_MAX) ? k_scale[id] : 0.f;
+}
+
+constexpr int kStatsThreads = 256;
+
+// Block-wide radix select of the r-th largest (1-based) of m uint32 values in
+// shared memory.  Returns the value.
+__device__ uint32_t block_select_u32(const uint32_t* vals, int m, int r, unsigned* hist256,
+                                     uint32_t* sh_state) {
+  uint32_t prefix = 0, mask = 0;
+  int remaining = r;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist256[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+      const uint32_t v = vals[i];
+      if ((v & mask) == prefix) atomicAdd(&hist256[(v >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int above = 0;
+      int digit = 0;
+      for (int dgt = 255; dgt >= 0; --dgt) {
+        const int c = static_cast<int>(hist256[dgt]);
+        if (above + c >= remaining) {
+          digit = dgt;
+          break;
+        }
+        above += c;
+      }
+      sh_state[0] = static_cast<uint32_t>(digit);
+      sh_state[1] = static_cast<uint32_t>(above);
+    }
+    __syncthreads();
+    prefix |= sh_state[0] << shift;
+    mask |= 0xFFu << shift;
+    remaining -= static_cast<int>(sh_state[1]);
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Per query: range of the visible sample scores, delta = nb / (s_max - s_min),
+// and the initial threshold bin = bin of the k-th largest visible sample score
+// minus one (one bin of slack so that a score computed in a different rounding
+// order could never lift the start above the true k-th score's bin).  With
+// fewer than k visible sample keys the threshold starts at 0.
+__global__ void __launch_bounds__(kStatsThreads) sample_stats_kernel(const SampleStatsParams p) {
+  extern __shared__ uint32_t s_ord[];
+  __shared__ unsigned hist256[256];
+  __shared__ uint32_t sh_state[2];
+  __shared__ float red_min[kStatsThreads / 32], red_max[kStatsThreads / 32];
+  __shared__ int red_cnt[kStatsThreads / 32];
+  const int t = blockIdx.x;
+  const float* row = p.scores + static_cast<size_t>(t) * p.ld;
+  float mn = INFINITY, mx = -INFINITY;
+  int cnt = 0;
+  for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
+    const float v = row[i];
+    const bool vis = v != -INFINITY;
+    s_ord[i] = vis ? ord_f32(v) : 0u;
+    if (vis) {
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+      ++cnt;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red_min[warp] = mn;
+    red_max[warp] = mx;
+    red_cnt[warp] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kStatsThreads / 32; ++w) {
+      mn = fminf(mn, red_min[w]);
+      mx = fmaxf(mx, red_max[w]);
+      cnt += red_cnt[w];
+    }
+    red_min[0] = mn;
+    red_max[0] = mx;
+    red_cnt[0] = cnt;
+  }
+  __syncthreads();
+  mn = red_min[0];
+  mx = red_max[0];
+  cnt = red_cnt[0];
+  float smin = 0.f, delta = 0.f;
+  if (cnt > 0) {
+    smin = mn;
+    if (mx > mn) {
+      delta = __fdiv_rn(static_cast<float>(p.nb), __fsub_rn(mx, mn));
+      if (!(delta <= 1e30f)) delta = 1e30f;
+    }
+  }
+  int theta = 0;
+  if (cnt >= p.k && p.k > 0) {
+    const uint32_t kth = block_select_u32(s_ord, p.n, p.k, hist256, sh_state);
+    theta = max(0, bin_of(unord_f32(kth), smin, delta, p.nb) - 1);
+  }
+  if (threadIdx.x == 0) {
+    p.s_min[t] = smin;
+    p.delta[t] = delta;
+    p.theta0[t] = theta;
+  }
+}
+
+// ---- previous-chunk sample: rank key ids by selection count ----
+__global__ void count_kernel(const int* __restrict__ prev, long long n_prev, long long S,
+                             int* __restrict__ counts) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_prev;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int id = prev[i];
+    if (id >= 0 && id < S) atomicAdd(&counts[id], 1);
+  }
+}
+
+// Ranking key: count in the high word; ties broken by the higher id among
+// selected keys, pseudo-randomly (a bijection of the id) among unselected ones.
+__global__ void rank_keys_kernel(const int* __restrict__ counts, long long S, unsigned long long seed,
+                                 unsigned long long* __restrict__ keys) {
+  for (long long s = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; s < S;
+       s += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint32_t c = static_cast<uint32_t>(counts[s]);
+    const uint32_t lo = c > 0 ? static_cast<uint32_t>(s) : perm31(static_cast<uint32_t>(s), seed);
+    keys[s] = (static_cast<uint64_t>(c) << 32) | lo;
+  }
+}
+
+// state: [0] prefix, [1] mask, [2] remaining, [3] output slot
+__global__ void digit_hist_kernel(const unsigned long long* __restrict__ keys, long long S, int shift,
+                                  const unsigned long long* __restrict__ state,
+                                  unsigned int* __restrict__ hist) {
+  __shared__ unsigned int h[256];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  const uint64_t prefix = state[0], mask = state[1];
+  for (long long s = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; s < S;
+       s += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint64_t k = keys[s];
+    if ((k & mask) == prefix) atomicAdd(&h[(k >> shift) & 255u], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    if (h[i]) atomicAdd(&hist[i], h[i]);
+}
+
+__global__ void digit_pick_kernel(unsigned int* hist, int shift, unsigned long long* state) {
+  if (threadIdx.x != 0) return;
+  const long long remaining = static_cast<long long>(state[2]);
+  long long above = 0;
+  int digit = 0;
+  for (int d = 255; d >= 0; --d) {
+    const long long c = hist[d];
+    if (above + c >= remaining) {
+      digit = d;
+      break;
+    }
+    above += c;
+  }
+  state[0] |= static_cast<uint64_t>(digit) << shift;
+  state[1] |= static_cast<uint64_t>(0xFF) << shift;
+  state[2] = static_cast<uint64_t>(remaining - above);
+  for (int d = 0; d < 256; ++d) hist[d] = 0;
+}
+
+__global__ void collect_top_kernel(const unsigned long long* __restrict__ keys, long long S,
+                                   unsigned long long* state, int n, int* __restrict__ out) {
+  const uint64_t kth = state[0];
+  for (long long s = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; s < S;
+       s += static_cast<long long>(gridDim.x) * blockDim.x) {
+    if (keys[s] >= kth) {
+      const unsigned long long slot = atomicAdd(&state[3], 1ull);
+      if (slot < static_cast<unsigned long long>(n)) out[slot] = static_cast<int>(s);
+    }
+  }
+}
+
+__global__ void init_select_state_kernel(unsigned long long* state, unsigned int* hist, int n) {
+  if (threadIdx.x == 0) {
+    state[0] = 0;
+    state[1] = 0;
+    state[2] = static_cast<unsigned long long>(n);
+    state[3] = 0;
+  }
+  for (int d = threadIdx.x; d < 256; d += blockDim.x) hist[d] = 0;
+}
+
+int grid_for(long long n, int threads, int cap_blocks) {
+  long long b = (n + threads - 1) / threads;
+  if (b < 1) b = 1;
+  if (b > cap_blocks) b = cap_blocks;
+  return static_cast<int>(b);
+}
+
+}  // namespace
+
+cudaError_t launch_random_sample(long long S, int n, unsigned long long seed, int* out,
+                                 cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  random_sample_kernel<<<(n + 255) / 256, 256, 0, stream>>>(S, n, seed, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_sample(const int* ids, int n, long long S, int n_pad, int* key_ids_pad,
+                                  cudaStream_t stream) {
+  int P = 1;
+  while (P < n) P <<= 1;
+  const size_t smem = static_cast<size_t>(P) * sizeof(int);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(prepare_sample_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMaxSample * sizeof(int)));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  prepare_sample_kernel<<<1, kPrepThreads, smem, stream>>>(ids, n, S, n_pad, key_ids_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int elem_bytes, int dim,
+                               const int* key_ids_pad, int n_pad, void* k_samp, float* k_scale_samp,
+                               cudaStream_t stream) {
+  const int vec = dim * elem_bytes / 16;
+  const long long total = static_cast<long long>(n_pad) * vec;
+  const int blocks = static_cast<int>((total + 255) / 256);
+  if (blocks == 0) return cudaSuccess;
+  gather_keys_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(k_cache), k_scale, vec,
+                                                 key_ids_pad, n_pad, static_cast<uint4*>(k_samp),
+                                                 k_scale_samp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sample_stats(const SampleStatsParams& p, cudaStream_t stream) {
+  if (p.T <= 0) return cudaSuccess;
+  const size_t smem = static_cast<size_t>(p.n) * sizeof(uint32_t);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(sample_stats_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMaxSample * sizeof(uint32_t)));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  sample_stats_kernel<<<p.T, kStatsThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_make_sample(const int* prev_idx, long long n_prev, long long S, int n,
+                               unsigned long long seed, const MakeSampleWs& ws, int* out,
+                               cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(ws.counts, 0, static_cast<size_t>(S) * sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  if (n_prev > 0) {
+    count_kernel<<<grid_for(n_prev, 256, 4096), 256, 0, stream>>>(prev_idx, n_prev, S, ws.counts);
+  }
+  rank_keys_kernel<<<grid_for(S, 256, 4096), 256, 0, stream>>>(ws.counts, S, seed, ws.keys);
+  init_select_state_kernel<<<1, 256, 0, stream>>>(ws.state, ws.hist, n);
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    digit_hist_kernel<<<grid_for(S, 256, 1024), 256, 0, stream>>>(ws.keys, S, shift, ws.state, ws.hist);
+    digit_pick_kernel<<<1, 32, 0, stream>>>(ws.hist, shift, ws.state);
+  }
+  collect_top_kernel<<<grid_for(S, 256, 4096), 256, 0, stream>>>(ws.keys, S, ws.state, n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace ltk

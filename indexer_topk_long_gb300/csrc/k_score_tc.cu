@@ -1,0 +1,436 @@
+// k_score_tc.cu -- tensor-core indexer scorer with the fused Filter epilogue.
+//
+// LiteTopK (gist.science technical summary), Methodology step 2 "Filtering":
+// scores are computed by tensor-core matrix multiplication while CUDA cores map
+// each score to a bin, keep it only if its bin is at or above the current
+// threshold bin ("Gatekeeping"), append kept candidates to warp-local batches
+// that are flushed with one atomic per batch ("Write-Back Optimization"), and
+// an otherwise idle warp recomputes the threshold bin from the top of the
+// histogram with a plain overwrite ("Threshold Refresh").
+//
+// GB300 design (one CTA per 8 queries, 12 warps):
+//   * Q tile: 8 queries x 64 heads x d=128 stays resident in shared memory
+//     (bf16 128 KB, e4m3 64 KB), loaded once by TMA with 128-byte swizzle.
+//   * K tiles of 128 keys stream through a TMA ring (bf16 2 x 32 KB, e4m3
+//     4 x 16 KB).
+//   * tcgen05.mma, cta_group::1, M = 128 keys, N = 256 = 4 queries x 64 heads:
+//     keys sit on TMEM lanes, so one epilogue thread owns one key row and the
+//     weighted head sum is intra-thread.  TMEM (512 columns) holds two
+//     accumulators, one per half of the query block; the epilogue drains one
+//     half while the tensor core fills the other.
+//   * Epilogue (8 warps): tcgen05.ld -> ReLU, w-weighted head sum (fp32 FMA)
+//     -> mask -> [dense: store I] or [filter: bin, gate, warp ballot append,
+//     shared-memory histogram].
+//   * Warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warp 2 =
+//     threshold refresh, warp 3 idle.
+// Every wait is bounded (2 s); on expiry the kernel records LTK_ERR_TIMEOUT,
+// drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <climits>
+#include <cmath>
+
+#include "ltk_internal.cuh"
+
+namespace ltk {
+namespace {
+
+template <bool FP8>
+struct Shape {
+  static constexpr int kChunks = FP8 ? 1 : 2;                 // 128-byte chunks along d
+  static constexpr int kKSteps = kChunks * 4;                 // MMA K steps (32 bytes each)
+  static constexpr int kQChunkBytes = kTcQPB * kTcHeads * 128;
+  static constexpr int kQBytes = kChunks * kQChunkBytes;      // 128 KB bf16 / 64 KB e4m3
+  static constexpr int kKChunkBytes = kTile * 128;
+  static constexpr int kKStage = kChunks * kKChunkBytes;      // 32 KB bf16 / 16 KB e4m3
+  static constexpr int kStages = FP8 ? 4 : 2;
+  static constexpr int kMaxBins = FP8 ? 2048 : 512;
+  static constexpr int kBoxCols = FP8 ? 128 : 64;             // elements per 128-byte box row
+};
+
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kRefreshWarp = 2;
+constexpr int kN = 256;                 // MMA N: 4 queries x 64 heads
+constexpr uint32_t kTmemCols = 512;
+
+struct __align__(8) Ctrl {
+  uint64_t q_full;
+  uint64_t k_full[4];
+  uint64_t k_empty[4];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int tiles_done;                        // epilogue warp-tiles finished
+  int pad0;
+  float s_min[kTcQPB];
+  float delta[kTcQPB];
+  int theta[kTcQPB];
+  int pos[kTcQPB];
+  int cnt[kTcQPB];
+};
+
+template <bool FP8>
+constexpr size_t smem_bytes(int nb) {
+  return 1024 /* alignment slack */ + Shape<FP8>::kQBytes +
+         static_cast<size_t>(Shape<FP8>::kStages) * Shape<FP8>::kKStage +
+         kTcQPB * kTcHeads * sizeof(float) + sizeof(Ctrl) +
+         static_cast<size_t>(kTcQPB) * nb * sizeof(int);
+}
+
+// sum_h w[h] * max(0, v[h]) in fp32, fixed order (4 interleaved partial sums).
+__device__ __forceinline__ float head_sum(const float* v, const float* w) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int h = 0; h < kTcHeads; h += 4) {
+    const float4 wv = *reinterpret_cast<const float4*>(w + h);
+    a0 = __fmaf_rn(fmaxf(v[h + 0], 0.f), wv.x, a0);
+    a1 = __fmaf_rn(fmaxf(v[h + 1], 0.f), wv.y, a1);
+    a2 = __fmaf_rn(fmaxf(v[h + 2], 0.f), wv.z, a2);
+    a3 = __fmaf_rn(fmaxf(v[h + 3], 0.f), wv.w, a3);
+  }
+  return __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
+}
+
+// Threshold refresh by one warp (Methodology step 2, "Threshold Refresh"):
+// accumulate the histogram from the top bin down and publish the highest bin b
+// whose cumulative count reaches k.  Counts only grow and each counted key is
+// distinct, so any b found is a valid lower bound on the bin of the true k-th
+// score; the store is a plain overwrite, never below the current value.
+__device__ __forceinline__ void refresh_threshold(const int* hist, int nb, int k,
+                                                  volatile int* theta, int lane) {
+  const volatile int* hv = hist;
+  const int per = nb >> 5;
+  const int hi = nb - lane * per;
+  const int lo = hi - per;
+  int seg = 0;
+  for (int b = lo; b < hi; ++b) seg += hv[b];
+  int cum = seg;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+    if (lane >= o) cum += n;
+  }
+  const unsigned m = __ballot_sync(0xFFFFFFFFu, cum >= k);
+  if (m == 0) return;
+  const int L = __ffs(m) - 1;
+  if (lane == L) {
+    int run = cum - seg;
+    int th = lo;
+    for (int b = hi - 1; b >= lo; --b) {
+      run += hv[b];
+      if (run >= k) {
+        th = b;
+        break;
+      }
+    }
+    if (th > *theta) *theta = th;
+  }
+}
+
+template <int MODE, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap q_map,
+                    const __grid_constant__ CUtensorMap k_map, const ScoreParams p) {
+  using Sh = Shape<FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t s_q = raw + pad;
+  const uint32_t s_k = s_q + Sh::kQBytes;
+  float* w_s = reinterpret_cast<float*>(smem + Sh::kQBytes + Sh::kStages * Sh::kKStage);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(w_s + kTcQPB * kTcHeads);
+  int* hist = reinterpret_cast<int*>(ctrl + 1);
+  volatile int* abort_flag = &ctrl->abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int t0 = blockIdx.x * kTcQPB;
+  const int nq = min(kTcQPB, p.T - t0);
+
+  // Keys to scan: up to the largest position in the block when causal.
+  long long last_row = p.rows;
+  if (p.causal && p.positions != nullptr && p.key_ids == nullptr) {
+    int mp = -1;
+    for (int i = 0; i < nq; ++i) mp = max(mp, p.positions[t0 + i]);
+    last_row = min(static_cast<long long>(mp) + 1, p.rows);
+    if (last_row < 0) last_row = 0;
+  }
+  const int n_tiles = static_cast<int>((last_row + kTile - 1) / kTile);
+
+  // ---- setup: weights, per-query state, histogram, barriers, TMEM
+  for (int i = tid; i < kTcQPB * kTcHeads; i += kThreads) {
+    const int ql = i / kTcHeads;
+    float wv = 0.f;
+    if (ql < nq) {
+      wv = p.w[static_cast<size_t>(t0 + ql) * kTcHeads + (i % kTcHeads)];
+      if constexpr (FP8) wv = __fmul_rn(wv, p.q_scale[t0 + ql]);
+    }
+    w_s[i] = wv;
+  }
+  if (tid < kTcQPB) {
+    const bool ok = tid < nq;
+    ctrl->pos[tid] = (ok && p.positions != nullptr) ? p.positions[t0 + tid] : INT_MAX;
+    ctrl->cnt[tid] = 0;
+    if constexpr (MODE == kModeFilter) {
+      ctrl->s_min[tid] = ok ? p.s_min[t0 + tid] : 0.f;
+      ctrl->delta[tid] = ok ? p.delta[t0 + tid] : 0.f;
+      ctrl->theta[tid] = ok ? p.theta0[t0 + tid] : 0;
+    }
+  }
+  if constexpr (MODE == kModeFilter) {
+    for (int i = tid; i < kTcQPB * p.nb; i += kThreads) hist[i] = 0;
+  }
+  if (tid == 0) {
+    ctrl->abort_flag = 0;
+    ctrl->tiles_done = 0;
+    mbar_init(smem_u32(&ctrl->q_full), 1);
+    for (int s = 0; s < Sh::kStages; ++s) {
+      mbar_init(smem_u32(&ctrl->k_full[s]), 1);
+      mbar_init(smem_u32(&ctrl->k_empty[s]), 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(smem_u32(&ctrl->acc_full[j]), 1);
+      mbar_init(smem_u32(&ctrl->acc_empty[j]), kEpiWarps);
+    }
+    mbar_init(smem_u32(&ctrl->mma_done), 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (n_tiles > 0) {
+    if (warp == 0) {
+      // ---------------- TMA producer ----------------
+      if (lane == 0) {
+        tma_prefetch_desc(&q_map);
+        tma_prefetch_desc(&k_map);
+        const uint32_t qbar = smem_u32(&ctrl->q_full);
+        mbar_arrive_expect_tx(qbar, Sh::kQBytes);
+        for (int j = 0; j < 2; ++j)
+          for (int c = 0; c < Sh::kChunks; ++c)
+            tma_load_2d(s_q + c * Sh::kQChunkBytes + j * (kN * 128), &q_map, c * Sh::kBoxCols,
+                        (t0 + 4 * j) * kTcHeads, qbar);
+        int issued[Sh::kStages];
+        for (int s = 0; s < Sh::kStages; ++s) issued[s] = -1;
+        for (int i = 0; i < n_tiles; ++i) {
+          const int s = i % Sh::kStages;
+          if (i >= Sh::kStages &&
+              !mbar_wait(smem_u32(&ctrl->k_empty[s]), ((i / Sh::kStages) - 1) & 1, abort_flag,
+                         p.status))
+            break;
+          const uint32_t fb = smem_u32(&ctrl->k_full[s]);
+          mbar_arrive_expect_tx(fb, Sh::kKStage);
+          for (int c = 0; c < Sh::kChunks; ++c)
+            tma_load_2d(s_k + s * Sh::kKStage + c * Sh::kKChunkBytes, &k_map, c * Sh::kBoxCols,
+                        i * kTile, fb);
+          issued[s] = i;
+        }
+        if (*abort_flag) {
+          // drain copies still in flight before the CTA may exit
+          mbar_drain(qbar, 0);
+          for (int s = 0; s < Sh::kStages; ++s)
+            if (issued[s] >= 0) mbar_drain(smem_u32(&ctrl->k_full[s]), (issued[s] / Sh::kStages) & 1);
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------- MMA issuer ----------------
+      if (lane == 0) {
+        const uint32_t idesc = make_idesc(FP8, kTile, kN);
+        bool ok = mbar_wait(smem_u32(&ctrl->q_full), 0, abort_flag, p.status);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          const int s = i % Sh::kStages;
+          if (!mbar_wait(smem_u32(&ctrl->k_full[s]), (i / Sh::kStages) & 1, abort_flag, p.status))
+            break;
+          tc_fence_after();
+          for (int j = 0; j < 2; ++j) {
+            if (i > 0) {
+              if (!mbar_wait(smem_u32(&ctrl->acc_empty[j]), (i - 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t d_tmem = tmem + j * kN;
+#pragma unroll
+            for (int ks = 0; ks < Sh::kKSteps; ++ks) {
+              const int c = ks >> 2;
+              const int kk = ks & 3;
+              const uint64_t a = smem_desc_sw128(s_k + s * Sh::kKStage + c * Sh::kKChunkBytes + kk * 32);
+              const uint64_t b = smem_desc_sw128(s_q + c * Sh::kQChunkBytes + j * (kN * 128) + kk * 32);
+              tc_mma<FP8>(d_tmem, a, b, idesc, ks > 0 ? 1u : 0u);
+            }
+            tc_commit(smem_u32(&ctrl->acc_full[j]));
+          }
+          if (!ok) break;
+          tc_commit(smem_u32(&ctrl->k_empty[s]));
+        }
+        // every MMA issued so far must finish before TMEM is freed
+        tc_commit(smem_u32(&ctrl->mma_done));
+        mbar_drain(smem_u32(&ctrl->mma_done), 0);
+      }
+    } else if (warp == kRefreshWarp) {
+      // ---------------- threshold refresh ----------------
+      if constexpr (MODE == kModeFilter) {
+        if (p.refresh_interval > 0) {
+          int last = 0;
+          int prev_done = -1;
+          uint64_t t_prog = globaltimer_ns();
+          while (true) {
+            int done = *reinterpret_cast<volatile int*>(&ctrl->tiles_done) / kEpiWarps;
+            done = __shfl_sync(0xFFFFFFFFu, done, 0);
+            const int ab = __shfl_sync(0xFFFFFFFFu, *abort_flag, 0);
+            if (done >= n_tiles || ab) break;
+            if (done != prev_done) {
+              prev_done = done;
+              t_prog = globaltimer_ns();
+            }
+            if (done - last >= p.refresh_interval) {
+              last = done;
+              for (int ql = 0; ql < nq; ++ql)
+                refresh_threshold(hist + ql * p.nb, p.nb, p.k,
+                                  reinterpret_cast<volatile int*>(&ctrl->theta[ql]), lane);
+            } else {
+              __nanosleep(200);
+              bool expired = globaltimer_ns() - t_prog > kWaitLimitNs;
+              expired = __shfl_sync(0xFFFFFFFFu, expired, 0);
+              if (expired) {
+                if (lane == 0) {
+                  *abort_flag = 1;
+                  raise_status(p.status, kDevTimeout);
+                }
+                break;
+              }
+            }
+          }
+        }
+      }
+    } else if (warp >= kEpiWarp0) {
+      // ---------------- epilogue ----------------
+      const int e = warp - kEpiWarp0;
+      const int lq = warp & 3;               // TMEM lane quarter this warp may access
+      const int qp = e >> 2;                 // which query pair of a half
+      const int row = lq * 32 + lane;
+      const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
+      for (int i = 0; i < n_tiles; ++i) {
+        const long long key = static_cast<long long>(i) * kTile + row;
+        const bool key_ok = key < p.rows;
+        float kscale = 1.f;
+        if constexpr (FP8) kscale = key_ok ? p.k_scale[key] : 0.f;
+        int kid = static_cast<int>(key);
+        if (MODE == kModeDense && p.key_ids != nullptr) kid = key_ok ? p.key_ids[key] : INT_MAX;
+        bool stop = false;
+        for (int j = 0; j < 2 && !stop; ++j) {
+          bool ok = mbar_wait(smem_u32(&ctrl->acc_full[j]), i & 1, abort_flag, p.status);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int qq = 0; qq < 2; ++qq) {
+            const int qh = qp * 2 + qq;         // query within the half
+            const int ql = j * 4 + qh;          // query within the CTA
+            float v[kTcHeads];
+            const uint32_t ta = tmem + lane_base + j * kN + qh * kTcHeads;
+            tmem_ld32(ta, v);
+            tmem_ld32(ta + 32, v + 32);
+            tmem_wait_ld();
+            if (qq == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[j]));
+            }
+            float I = head_sum(v, w_s + ql * kTcHeads);
+            if constexpr (FP8) I = __fmul_rn(I, kscale);
+            if constexpr (MODE == kModeDense) {
+              if (ql < nq && key_ok) {
+                bool vis = kid != INT_MAX;
+                if (p.causal && p.positions != nullptr) vis = vis && kid <= ctrl->pos[ql];
+                p.dense[static_cast<size_t>(t0 + ql) * p.ld + key] = vis ? I : -INFINITY;
+              }
+            } else {
+              const bool vis = (ql < nq) && key_ok && (!p.causal || key <= ctrl->pos[ql]);
+              const int b = bin_of(I, ctrl->s_min[ql], ctrl->delta[ql], p.nb);
+              const int th = *reinterpret_cast<volatile int*>(&ctrl->theta[ql]);
+              const bool pass = vis && b >= th;
+              const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
+              if (m != 0) {
+                const int leader = __ffs(m) - 1;
+                int base = 0;
+                if (lane == leader) base = atomicAdd(&ctrl->cnt[ql], __popc(m));
+                base = __shfl_sync(0xFFFFFFFFu, base, leader);
+                if (pass) {
+                  const int slot = base + __popc(m & ((1u << lane) - 1u));
+                  if (slot < p.cap)
+                    p.cand[static_cast<size_t>(t0 + ql) * p.cap + slot] =
+                        cand_pack(I, static_cast<int>(key));
+                  atomicAdd(&hist[ql * p.nb + b], 1);
+                }
+              }
+            }
+          }
+        }
+        if (stop) break;
+        if (lane == 0) atomicAdd(&ctrl->tiles_done, 1);
+      }
+    }
+  }
+
+  // ---- teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if constexpr (MODE == kModeFilter) {
+    if (tid < nq) p.cnt[t0 + tid] = ctrl->cnt[tid];
+  }
+}
+
+template <int MODE, bool FP8>
+cudaError_t launch_one(const CUtensorMap& qm, const CUtensorMap& km, const ScoreParams& p,
+                       cudaStream_t stream) {
+  const int grid = (p.T + kTcQPB - 1) / kTcQPB;
+  if (grid == 0) return cudaSuccess;
+  const size_t smem = smem_bytes<FP8>(MODE == kModeFilter ? p.nb : 0);
+  static size_t configured = 0;
+  if (configured < smem) {
+    cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<MODE, FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<FP8>(Shape<FP8>::kMaxBins)));
+    if (e != cudaSuccess) return e;
+    configured = smem_bytes<FP8>(Shape<FP8>::kMaxBins);
+  }
+  score_tc_kernel<MODE, FP8><<<grid, kThreads, smem, stream>>>(qm, km, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t score_tc_smem_bytes(int mode, bool fp8, int nb) {
+  const int b = mode == kModeFilter ? nb : 0;
+  return fp8 ? smem_bytes<true>(b) : smem_bytes<false>(b);
+}
+
+int score_tc_max_bins(bool fp8) { return fp8 ? Shape<true>::kMaxBins : Shape<false>::kMaxBins; }
+
+cudaError_t launch_score_tc(int mode, bool fp8, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                            const ScoreParams& p, cudaStream_t stream) {
+  if (mode == kModeDense)
+    return fp8 ? launch_one<kModeDense, true>(q_map, k_map, p, stream)
+               : launch_one<kModeDense, false>(q_map, k_map, p, stream);
+  return fp8 ? launch_one<kModeFilter, true>(q_map, k_map, p, stream)
+             : launch_one<kModeFilter, false>(q_map, k_map, p, stream);
+}
+
+}  // namespace ltk

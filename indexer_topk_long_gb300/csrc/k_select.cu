@@ -1,0 +1,585 @@
+// k_select.cu -- the Select stage, the decoupled baseline's selection and the
+// overflow rescue.
+//
+// LiteTopK technical summary, Methodology step 3 "Selection (Finalization)":
+// once the scan is over, candidates in bins strictly above the final
+// threshold bin go straight to the output, and a standard exact top-k runs
+// only over the candidates inside the final threshold bin.
+//
+// The Filter stage stores the raw fp32 score of every kept candidate, so no
+// inverse affine map is needed to recover scores: the output score is the
+// kernel's own fp32 score.  Select re-bins the candidate list over its own
+// [min, max] range with finer bins; any monotone bin map gives the same exact
+// result because the list holds every key whose score reaches the k-th one.
+//
+// Ordering everywhere is the composite key (score desc, index asc), so ties at
+// the k-th score go to the lower key index and the result is unique.
+//
+// Also here: the decoupled baseline's row radix select (the DSA-style design
+// of the summary's Problem Statement: select over a fully materialised score
+// row, reading it several times), and the rescue of queries whose candidate
+// list overflowed: their full row is recomputed on CUDA cores into a scratch
+// row and selected with the same row radix select.
+#include <climits>
+#include <cmath>
+
+#include "ltk_internal.cuh"
+
+namespace ltk {
+namespace {
+
+constexpr int kSelThreads = 512;
+constexpr int kBndCap = 4096;        // boundary-bin entries held in shared memory
+
+// ---------------------------------------------------------------------------
+// Block helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_min(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < (blockDim.x >> 5); ++i) r = fminf(r, red[i]);
+  return r;
+}
+__device__ __forceinline__ float block_max(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < (blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
+  return r;
+}
+
+// Descending bitonic sort of P (power of two) 64-bit keys in shared memory.
+__device__ void bitonic_desc_u64(unsigned long long* a, int P) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const unsigned long long x = a[lo], y = a[hi];
+        if ((x < y) == desc) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Pick the digit holding the r-th largest: 256-bin histogram, scanned top
+// down by warp 0.  Writes (digit, count strictly above it) to sh[0..1].
+__device__ __forceinline__ void pick_digit(const unsigned* hist256, long long remaining,
+                                           long long* sh) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    // lane l owns digits [255 - 8l - 7, 255 - 8l]
+    long long seg = 0;
+    for (int j = 0; j < 8; ++j) seg += hist256[255 - 8 * lane - j];
+    long long cum = seg;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long n = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+      if (lane >= o) cum += n;
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, cum >= remaining);
+    const int L = m ? __ffs(m) - 1 : 31;
+    if (lane == L) {
+      long long above = cum - seg;
+      int digit = 255 - 8 * L - 7;
+      for (int j = 0; j < 8; ++j) {
+        const int d = 255 - 8 * L - j;
+        const long long c = hist256[d];
+        if (above + c >= remaining) {
+          digit = d;
+          break;
+        }
+        above += c;
+      }
+      sh[0] = digit;
+      sh[1] = above;
+    }
+  }
+  __syncthreads();
+}
+
+// r-th largest (1-based) of m distinct 64-bit keys in shared memory.
+__device__ unsigned long long select_u64_smem(const unsigned long long* keys, int m, int r,
+                                              unsigned* hist256, long long* sh) {
+  unsigned long long prefix = 0, mask = 0;
+  long long remaining = r;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist256[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+      const unsigned long long k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&hist256[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    pick_digit(hist256, remaining, sh);
+    prefix |= static_cast<unsigned long long>(sh[0]) << shift;
+    mask |= 0xFFull << shift;
+    remaining -= sh[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// r-th largest composite key among the list entries whose select-bin is `bin`
+// (global-memory variant for a boundary bin too large for shared memory).
+__device__ unsigned long long select_u64_list(const unsigned long long* list, int n, float lo,
+                                              float delta, int bin, int r, unsigned* hist256,
+                                              long long* sh) {
+  unsigned long long prefix = 0, mask = 0;
+  long long remaining = r;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist256[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const unsigned long long c = list[i];
+      const float s = cand_score(c);
+      if (bin_of(s, lo, delta, kSelBins) != bin) continue;
+      const unsigned long long k = ckey(s, cand_idx(c));
+      if ((k & mask) == prefix) atomicAdd(&hist256[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    pick_digit(hist256, remaining, sh);
+    prefix |= static_cast<unsigned long long>(sh[0]) << shift;
+    mask |= 0xFFull << shift;
+    remaining -= sh[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+__device__ __forceinline__ int visible_of(const int* positions, int t, long long S, int causal) {
+  if (!causal || positions == nullptr) return static_cast<int>(S);
+  const long long v = static_cast<long long>(positions[t]) + 1;
+  return static_cast<int>(v < 0 ? 0 : (v > S ? S : v));
+}
+
+// Sort the kk selected keys (buffer padded to P with 0) and write the row.
+__device__ void write_sorted(unsigned long long* buf, int kk, int k, int t, int* out_idx,
+                             float* out_score) {
+  int P = 1;
+  while (P < kk) P <<= 1;
+  for (int i = kk + threadIdx.x; i < P; i += blockDim.x) buf[i] = 0ull;
+  __syncthreads();
+  bitonic_desc_u64(buf, P);
+  int* oi = out_idx + static_cast<size_t>(t) * k;
+  float* os = out_score + static_cast<size_t>(t) * k;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    if (i < kk) {
+      oi[i] = ckey_idx(buf[i]);
+      os[i] = ckey_score(buf[i]);
+    } else {
+      oi[i] = -1;
+      os[i] = -INFINITY;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Select stage (fused path), one CTA per query
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
+  extern __shared__ unsigned long long sel_smem[];
+  __shared__ int hist[kSelBins];
+  __shared__ unsigned hist256[256];
+  __shared__ long long sh[2];
+  __shared__ float red[kSelThreads / 32];
+  __shared__ int sh_int[4];   // theta_f, c_above, n_out, n_bnd
+
+  const int t = blockIdx.x;
+  const int V = visible_of(p.positions, t, p.S, p.causal);
+  const int kk = min(p.k, V);
+  const int n_raw = p.cnt[t];
+  if (n_raw > p.cap) {
+    if (threadIdx.x == 0) {
+      const int slot = atomicAdd(p.ovf_count, 1);
+      p.ovf_list[slot] = t;
+    }
+    return;
+  }
+  int P = 1;
+  while (P < max(kk, 1)) P <<= 1;
+  unsigned long long* outbuf = sel_smem;          // [P]
+  unsigned long long* bnd = sel_smem + P;         // [kBndCap]
+  const int n = n_raw;
+  const unsigned long long* list = p.cand + static_cast<size_t>(t) * p.cap;
+  if (kk == 0 || n == 0) {
+    write_sorted(outbuf, 0, p.k, t, p.out_idx, p.out_score);
+    return;
+  }
+
+  // pass A: range of the retained scores
+  float mn = INFINITY, mx = -INFINITY;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float s = cand_score(list[i]);
+    mn = fminf(mn, s);
+    mx = fmaxf(mx, s);
+  }
+  const float lo = block_min(mn, red);
+  const float hi = block_max(mx, red);
+  float delta = 0.f;
+  if (hi > lo) {
+    delta = __fdiv_rn(static_cast<float>(kSelBins), __fsub_rn(hi, lo));
+    if (!(delta <= 1e30f)) delta = 1e30f;
+  }
+
+  // pass B: histogram of the retained list
+  for (int i = threadIdx.x; i < kSelBins; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    atomicAdd(&hist[bin_of(cand_score(list[i]), lo, delta, kSelBins)], 1);
+  __syncthreads();
+
+  // final threshold bin: highest b with count(>= b) >= kk (warp 0, top down)
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = kSelBins / 32;
+    const int top = kSelBins - lane * per;
+    int seg = 0;
+    for (int b = top - per; b < top; ++b) seg += hist[b];
+    int cum = seg;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+      if (lane >= o) cum += v;
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, cum >= kk);
+    const int L = m ? __ffs(m) - 1 : 31;
+    if (lane == L) {
+      int above = cum - seg;
+      int th = top - per;
+      for (int b = top - 1; b >= top - per; --b) {
+        if (above + hist[b] >= kk) {
+          th = b;
+          break;
+        }
+        above += hist[b];
+      }
+      sh_int[0] = th;
+      sh_int[1] = above;   // candidates in bins strictly above th
+      sh_int[2] = 0;
+      sh_int[3] = 0;
+    }
+  }
+  __syncthreads();
+  const int theta_f = sh_int[0];
+  const int c_above = min(sh_int[1], kk);
+  const int r = kk - c_above;
+
+  // pass C: bins above go straight to the output; the boundary bin is staged
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned long long c = list[i];
+    const float s = cand_score(c);
+    const int b = bin_of(s, lo, delta, kSelBins);
+    if (b > theta_f) {
+      const int slot = atomicAdd(&sh_int[2], 1);
+      if (slot < kk) outbuf[slot] = ckey(s, cand_idx(c));
+    } else if (b == theta_f) {
+      const int slot = atomicAdd(&sh_int[3], 1);
+      if (slot < kBndCap) bnd[slot] = ckey(s, cand_idx(c));
+    }
+  }
+  __syncthreads();
+  const int m_bnd = sh_int[3];
+
+  // exact top-r inside the boundary bin
+  if (r > 0) {
+    unsigned long long kth;
+    if (m_bnd <= kBndCap) {
+      kth = select_u64_smem(bnd, m_bnd, r, hist256, sh);
+      for (int i = threadIdx.x; i < m_bnd; i += blockDim.x)
+        if (bnd[i] >= kth) {
+          const int slot = atomicAdd(&sh_int[2], 1);
+          if (slot < kk) outbuf[slot] = bnd[i];
+        }
+    } else {
+      kth = select_u64_list(list, n, lo, delta, theta_f, r, hist256, sh);
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const unsigned long long c = list[i];
+        const float s = cand_score(c);
+        if (bin_of(s, lo, delta, kSelBins) != theta_f) continue;
+        const unsigned long long key = ckey(s, cand_idx(c));
+        if (key >= kth) {
+          const int slot = atomicAdd(&sh_int[2], 1);
+          if (slot < kk) outbuf[slot] = key;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  write_sorted(outbuf, min(sh_int[2], kk), p.k, t, p.out_idx, p.out_score);
+}
+
+// ---------------------------------------------------------------------------
+// Row top-k over a materialised score row (decoupled baseline and rescue)
+// ---------------------------------------------------------------------------
+// Radix select over the fp32 scores' order-preserving codes, 8 bits per pass,
+// reading the row from device memory once per pass; then one collection pass:
+// scores above the k-th go to the output, and among scores equal to the k-th
+// the lowest indices are kept (ordered scan).
+__device__ void row_topk_block(const float* row, int V, int kk, int k, int t, int* out_idx,
+                               float* out_score, unsigned long long* outbuf, unsigned* hist256,
+                               long long* sh, int* sh_int) {
+  if (kk <= 0) {
+    write_sorted(outbuf, 0, k, t, out_idx, out_score);
+    return;
+  }
+  uint32_t prefix = 0, mask = 0;
+  long long remaining = kk;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist256[i] = 0;
+    __syncthreads();
+    if (vec) {
+      const int nv = V >> 2;
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        const float4 x = r4[i];
+        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t o = ord_f32(xs[j]);
+          if ((o & mask) == prefix) atomicAdd(&hist256[(o >> shift) & 255u], 1u);
+        }
+      }
+      for (int i = (nv << 2) + threadIdx.x; i < V; i += blockDim.x) {
+        const uint32_t o = ord_f32(row[i]);
+        if ((o & mask) == prefix) atomicAdd(&hist256[(o >> shift) & 255u], 1u);
+      }
+    } else {
+      for (int i = threadIdx.x; i < V; i += blockDim.x) {
+        const uint32_t o = ord_f32(row[i]);
+        if ((o & mask) == prefix) atomicAdd(&hist256[(o >> shift) & 255u], 1u);
+      }
+    }
+    __syncthreads();
+    pick_digit(hist256, remaining, sh);
+    prefix |= static_cast<uint32_t>(sh[0]) << shift;
+    mask |= 0xFFu << shift;
+    remaining -= sh[1];
+    __syncthreads();
+  }
+  const uint32_t kth = prefix;
+  const int need_ties = static_cast<int>(remaining);   // entries equal to kth to keep
+  if (threadIdx.x == 0) {
+    sh_int[0] = 0;   // output slot
+    sh_int[1] = 0;   // ties taken so far
+  }
+  __syncthreads();
+  // scores strictly above the k-th: anywhere in the row
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float s = row[i];
+    if (ord_f32(s) > kth) {
+      const int slot = atomicAdd(&sh_int[0], 1);
+      if (slot < kk) outbuf[slot] = ckey(s, i);
+    }
+  }
+  __syncthreads();
+  // ties at the k-th score: lowest indices first (ordered chunks)
+  __shared__ int warp_cnt[kSelThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int base = 0; base < V; base += blockDim.x) {
+    if (sh_int[1] >= need_ties) break;
+    const int i = base + threadIdx.x;
+    const bool tie = i < V && ord_f32(row[i]) == kth;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, tie);
+    if (lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < nw; ++w) {
+      if (w < warp) before += warp_cnt[w];
+      total += warp_cnt[w];
+    }
+    const int rank = sh_int[1] + before + __popc(m & ((1u << lane) - 1u));
+    if (tie && rank < need_ties) {
+      const int slot = atomicAdd(&sh_int[0], 1);
+      if (slot < kk) outbuf[slot] = ckey(row[i], i);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) sh_int[1] += total;
+    __syncthreads();
+  }
+  __syncthreads();
+  write_sorted(outbuf, min(sh_int[0], kk), k, t, out_idx, out_score);
+}
+
+__global__ void __launch_bounds__(kSelThreads) row_topk_kernel(const RowTopkParams p) {
+  extern __shared__ unsigned long long rt_smem[];
+  __shared__ unsigned hist256[256];
+  __shared__ long long sh[2];
+  __shared__ int sh_int[2];
+  const int t = blockIdx.x;
+  const int V = visible_of(p.positions, t, p.S, p.causal);
+  const int kk = min(p.k, V);
+  row_topk_block(p.rows + static_cast<size_t>(t) * p.ld, V, kk, p.k, t, p.out_idx, p.out_score,
+                 rt_smem, hist256, sh, sh_int);
+}
+
+// ---------------------------------------------------------------------------
+// Overflow rescue: CUDA-core recompute of a full score row, then row top-k
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  // OCP fp8 E4M3: sign, 4-bit exponent (bias 7), 3-bit mantissa; exponent 0
+  // is subnormal (m * 2^-9).  NaN codes do not occur in valid inputs.
+  const uint32_t sgn = (c & 0x80u) << 24;
+  const uint32_t e = (c >> 3) & 0xFu;
+  const uint32_t m = c & 0x7u;
+  float v;
+  if (e == 0) {
+    v = static_cast<float>(m) * 0.001953125f;   // exact: m * 2^-9
+  } else {
+    v = __uint_as_float(((e + 120u) << 23) | (m << 20));
+  }
+  return __uint_as_float(__float_as_uint(v) | sgn);
+}
+
+constexpr int kRescueThreads = 256;
+
+__device__ void rescue_row_scores(const RescueParams& p, int t, int V, float* row, float* qf,
+                                  float* wf) {
+  const int H = kTcHeads, d = kTcDim;
+  const size_t qoff = static_cast<size_t>(t) * H * d;
+  for (int i = threadIdx.x; i < H * d; i += blockDim.x) {
+    float v;
+    if (p.fp8) {
+      v = e4m3_value(static_cast<const uint8_t*>(p.q)[qoff + i]);
+    } else {
+      const uint16_t b = static_cast<const uint16_t*>(p.q)[qoff + i];
+      v = __uint_as_float(static_cast<uint32_t>(b) << 16);
+    }
+    qf[i] = v;
+  }
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    float wv = p.w[static_cast<size_t>(t) * H + h];
+    if (p.fp8) wv = __fmul_rn(wv, p.q_scale[t]);
+    wf[h] = wv;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < V; s += blockDim.x) {
+    float acc[kTcHeads];
+#pragma unroll
+    for (int h = 0; h < kTcHeads; ++h) acc[h] = 0.f;
+    for (int dc = 0; dc < d; dc += 16) {
+      float kv[16];
+      if (p.fp8) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.k_cache) +
+                                                           static_cast<size_t>(s) * d + dc);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) kv[j] = e4m3_value((w4[j >> 2] >> (8 * (j & 3))) & 0xFFu);
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_cache) +
+                                                          static_cast<size_t>(s) * d + dc);
+        const uint4 r0 = src[0], r1 = src[1];
+        const uint32_t w8[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          kv[2 * j] = __uint_as_float(w8[j] << 16);
+          kv[2 * j + 1] = __uint_as_float(w8[j] & 0xFFFF0000u);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kTcHeads; ++h) {
+        const float* qh = qf + h * d + dc;
+        float a = acc[h];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a = __fmaf_rn(qh[j], kv[j], a);
+        acc[h] = a;
+      }
+    }
+    float I = 0.f;
+#pragma unroll
+    for (int h = 0; h < kTcHeads; ++h) I = __fmaf_rn(p.relu ? fmaxf(acc[h], 0.f) : acc[h], wf[h], I);
+    if (p.fp8) I = __fmul_rn(I, p.k_scale[s]);
+    row[s] = I;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kRescueThreads) rescue_kernel(const RescueParams p) {
+  extern __shared__ unsigned long long rs_smem[];
+  __shared__ unsigned hist256[256];
+  __shared__ long long sh[2];
+  __shared__ int sh_int[2];
+  __shared__ int s_slot;
+  __shared__ float wf[kTcHeads];
+  float* qf = reinterpret_cast<float*>(rs_smem);   // [H*d] fp32, reused as output buffer later
+  float* row = p.scratch + static_cast<size_t>(blockIdx.x) * p.scratch_ld;
+  while (true) {
+    if (threadIdx.x == 0) s_slot = atomicAdd(p.ovf_next, 1);
+    __syncthreads();
+    const int slot = s_slot;
+    __syncthreads();
+    if (slot >= *p.ovf_count) break;
+    const int t = p.ovf_list[slot];
+    const int V = visible_of(p.positions, t, p.S, p.causal);
+    const int kk = min(p.k, V);
+    rescue_row_scores(p, t, V, row, qf, wf);
+    row_topk_block(row, V, kk, p.k, t, p.out_idx, p.out_score, rs_smem, hist256, sh, sh_int);
+    __syncthreads();
+  }
+}
+
+size_t outbuf_bytes(int k) {
+  int P = 1;
+  while (P < k) P <<= 1;
+  return static_cast<size_t>(P) * sizeof(unsigned long long);
+}
+
+}  // namespace
+
+cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
+  if (p.T <= 0) return cudaSuccess;
+  const size_t smem = outbuf_bytes(p.k) + kBndCap * sizeof(unsigned long long);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(outbuf_bytes(kMaxK) +
+                                                          kBndCap * sizeof(unsigned long long)));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  select_kernel<<<p.T, kSelThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream) {
+  if (p.T <= 0) return cudaSuccess;
+  const size_t smem = outbuf_bytes(p.k);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(row_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(outbuf_bytes(kMaxK)));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  row_topk_kernel<<<p.T, kSelThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rescue(const RescueParams& p, int rescue_rows, cudaStream_t stream) {
+  if (p.T <= 0 || rescue_rows <= 0) return cudaSuccess;
+  const size_t qbytes = static_cast<size_t>(kTcHeads) * kTcDim * sizeof(float);
+  const size_t smem = qbytes > outbuf_bytes(p.k) ? qbytes : outbuf_bytes(p.k);
+  static bool configured = false;
+  if (!configured) {
+    const size_t mx = qbytes > outbuf_bytes(kMaxK) ? qbytes : outbuf_bytes(kMaxK);
+    cudaError_t e = cudaFuncSetAttribute(rescue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(mx));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  rescue_kernel<<<rescue_rows, kRescueThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ltk

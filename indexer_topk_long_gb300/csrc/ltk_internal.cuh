@@ -1,0 +1,388 @@
+// ltk_internal.cuh -- internal declarations and device helpers of libltk.
+//
+// Hand-written PTX wrappers for sm_103a (mbarrier, TMA, tcgen05/TMEM), the bin
+// map of the Filter stage, order-preserving composite keys used by every
+// selection, and the launch functions each kernel file exports to the host
+// orchestration in ltk_api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ltk.h"
+
+namespace ltk {
+
+// ---------------------------------------------------------------------------
+// Limits and fixed shapes
+// ---------------------------------------------------------------------------
+constexpr int kMaxK = 8192;             // largest k a handle may request
+constexpr int kMaxSample = 16384;       // largest sample (k') a call may use
+constexpr int kTile = 128;              // keys per tensor-core tile (MMA M)
+constexpr int kTcHeads = 64;            // H of the tensor-core indexer path
+constexpr int kTcDim = 128;             // d of the tensor-core indexer path
+constexpr int kTcQPB = 8;               // queries per CTA of the scorer
+constexpr int kSelBins = 2048;          // bins of the Select stage's re-binning
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+// Device status word values (same numbering as ltk_status).
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 5;
+
+// ---------------------------------------------------------------------------
+// Small device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Record the first device error (later ones are dropped).
+__device__ __forceinline__ void raise_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Gate bin of a score (LiteTopK Methodology step 2, "Bin Mapping": the
+// affine map B = (I - s_min) * delta, delta = bins per unit score).
+// Rounded to nearest in fp32 and floored, then clamped to [0, nb-1]; NaN maps
+// to 0.  The map is monotone non-decreasing in I, and this one function is
+// used by the Sample, Filter and Select stages alike.
+__device__ __forceinline__ int bin_of(float I, float s_min, float delta, int nb) {
+  const float f = __fmul_rn(__fsub_rn(I, s_min), delta);
+  if (!(f >= 0.f)) return 0;
+  if (f >= static_cast<float>(nb)) return nb - 1;
+  return static_cast<int>(f);
+}
+
+// Order-preserving map fp32 -> uint32 (larger float -> larger integer).
+__device__ __forceinline__ uint32_t ord_f32(float f) {
+  if (f == 0.f) f = 0.f;   // -0 and +0 compare equal; give them one code
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unord_f32(uint32_t o) {
+  const uint32_t b = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(b);
+}
+
+// Composite key of the exact order: larger key = higher score, then lower
+// index.  Keys of distinct indices are distinct.
+__device__ __forceinline__ uint64_t ckey(float score, int idx) {
+  return (static_cast<uint64_t>(ord_f32(score)) << 32) |
+         static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(idx));
+}
+__device__ __forceinline__ int ckey_idx(uint64_t key) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
+}
+__device__ __forceinline__ float ckey_score(uint64_t key) {
+  return unord_f32(static_cast<uint32_t>(key >> 32));
+}
+
+// Candidate record written by the Filter stage: raw fp32 score and key index.
+__device__ __forceinline__ uint64_t cand_pack(float score, int idx) {
+  return (static_cast<uint64_t>(__float_as_uint(score)) << 32) | static_cast<uint32_t>(idx);
+}
+__device__ __forceinline__ float cand_score(uint64_t c) {
+  return __uint_as_float(static_cast<uint32_t>(c >> 32));
+}
+__device__ __forceinline__ int cand_idx(uint64_t c) {
+  return static_cast<int>(static_cast<uint32_t>(c & 0xFFFFFFFFull));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier (shared::cta)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the completion of phase `parity`.  Returns false when the
+// CTA's abort flag is set by another role or when the wait exceeds
+// kWaitLimitNs (then it sets the abort flag and the device status itself).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  for (int i = 0; i < 32; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (abort_flag != nullptr) *abort_flag = 1;
+      raise_status(status, kDevTimeout);
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight copies).
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor), tiled 2-D loads completing on an mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 / TMEM
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_slot),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, one instruction, issued by one
+// thread.  kind::f16 covers bf16 operands; kind::f8f6f4 covers e4m3.
+template <bool FP8>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  if constexpr (FP8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// Arrive on an mbarrier once every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored in the
+// 128-byte-swizzled layout that a TMA load with CU_TENSOR_MAP_SWIZZLE_128B
+// produces: rows of 128 bytes, 8-row atoms of 1024 bytes (stride-dimension
+// byte offset 1024), atom base 1024-byte aligned.  Fields (PTX ISA, tcgen05
+// shared memory descriptor): start address >> 4 in bits 0-13, leading-dim
+// byte offset >> 4 in 16-29 (unused for swizzled K-major), stride-dim byte
+// offset >> 4 in 32-45, fixed 0b001 in 46-48, base offset 0, swizzle mode in
+// 61-63 (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor (PTX ISA, tcgen05 instruction descriptor for
+// kind::f16 / kind::f8f6f4): D format f32 (bits 4-5 = 1), A/B format in bits
+// 7-9 / 10-12 (bf16 = 1 under kind::f16, e4m3 = 0 under kind::f8f6f4), both
+// operands K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(bool fp8, int M, int N) {
+  return (1u << 4) | ((fp8 ? 0u : 1u) << 7) | ((fp8 ? 0u : 1u) << 10) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel parameter blocks and launch functions (defined in the kernel files)
+// ---------------------------------------------------------------------------
+enum ScoreMode { kModeDense = 0, kModeFilter = 1 };
+
+struct ScoreParams {
+  const float* w;          // [T, H]
+  const float* q_scale;    // [T] (fp8) or null
+  const float* k_scale;    // [rows] (fp8) or null
+  const int* positions;    // [T] or null (no mask)
+  const int* key_ids;      // [rows] key id of each row (gathered sample), or null
+  int T;
+  long long rows;          // rows of the key source
+  int causal;
+  // Filter stage
+  const float* s_min;      // [T]
+  const float* delta;      // [T]
+  const int* theta0;       // [T]
+  unsigned long long* cand;  // [T, cap]
+  int* cnt;                // [T]
+  int cap;
+  int nb;
+  int k;
+  int refresh_interval;
+  // Dense output
+  float* dense;            // [T, ld]
+  long long ld;
+  int* status;
+};
+
+// Tensor-core scorer (k_score_tc.cu).  q_map/k_map are tiled TMA maps built by
+// make_q_map/make_k_map.
+cudaError_t launch_score_tc(int mode, bool fp8, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                            const ScoreParams& p, cudaStream_t stream);
+size_t score_tc_smem_bytes(int mode, bool fp8, int nb);
+int score_tc_max_bins(bool fp8);
+
+struct SampleStatsParams {
+  const float* scores;     // [T, ld] sample scores (-inf = invisible)
+  long long ld;
+  int n;                   // valid sample columns
+  int T;
+  int k;
+  int nb;
+  float* s_min;
+  float* delta;
+  int* theta0;
+};
+
+// Sample stage (k_sample.cu).
+cudaError_t launch_random_sample(long long S, int n, unsigned long long seed, int* out,
+                                 cudaStream_t stream);
+cudaError_t launch_prepare_sample(const int* ids, int n, long long S, int n_pad, int* key_ids_pad,
+                                  cudaStream_t stream);
+cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int elem_bytes, int dim,
+                               const int* key_ids_pad, int n_pad, void* k_samp, float* k_scale_samp,
+                               cudaStream_t stream);
+cudaError_t launch_sample_stats(const SampleStatsParams& p, cudaStream_t stream);
+
+struct MakeSampleWs {
+  int* counts;                  // [max_S]
+  unsigned long long* keys;     // [max_S]
+  unsigned int* hist;           // [256]
+  unsigned long long* state;    // [4]: prefix, mask, remaining, slot
+};
+cudaError_t launch_make_sample(const int* prev_idx, long long n_prev, long long S, int n,
+                               unsigned long long seed, const MakeSampleWs& ws, int* out,
+                               cudaStream_t stream);
+
+struct SelectParams {
+  const unsigned long long* cand;  // [T, cap]
+  const int* cnt;                  // [T]
+  const int* positions;            // [T] or null
+  int T;
+  long long S;
+  int causal;
+  int cap;
+  int k;
+  int* out_idx;                    // [T, k]
+  float* out_score;                // [T, k]
+  int* ovf_count;
+  int* ovf_list;                   // [T]
+};
+
+struct RowTopkParams {
+  const float* rows;               // [T, ld] scores (decoupled) or scratch rows
+  long long ld;
+  const int* positions;
+  int T;
+  long long S;
+  int causal;
+  int k;
+  int* out_idx;
+  float* out_score;
+};
+
+struct RescueParams {
+  const void* q;
+  const float* q_scale;
+  const float* w;
+  const void* k_cache;
+  const float* k_scale;
+  const int* positions;
+  int T;
+  long long S;
+  int causal;
+  int relu;
+  int heads;
+  int dim;
+  int fp8;
+  int k;
+  const int* ovf_count;
+  const int* ovf_list;
+  int* ovf_next;
+  float* scratch;                  // [rescue_rows, S]
+  long long scratch_ld;
+  int* out_idx;
+  float* out_score;
+};
+
+// Select stage, decoupled baseline selection and overflow rescue (k_select.cu).
+cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
+cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream);
+cudaError_t launch_rescue(const RescueParams& p, int rescue_rows, cudaStream_t stream);
+
+}  // namespace ltk
