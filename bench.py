@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused Indexer-TopK (LiteTopK-style) on one GB300.
+
+Workload (default): one 8192-query prefill chunk at 1M context -- queries at
+positions 1040384..1048575, S = 1048576 keys, H = 64, d = 128, k = 2048,
+bf16 q/k, fp32 w -- with the previous chunk's top-3k as the sample.  A step is
+one pass of the whole path: the previous-chunk sample (ltk_make_sample) plus
+the fused Sample -> Filter -> Select call (ltk_indexer_topk).
+
+Printed (rank 0, one JSON line): scored (visible) query-key pairs/s over the
+timed steps, ms per chunk, the score kernel's roofline fraction (CUDA events
+around that kernel on its launch stream, inside the timed region), the
+end-to-end number through the host-buffer C-ABI call, SM clocks sampled during
+the timed region, the same-GPU decoupled baseline, and the CPU oracle baseline.
+
+``--impl reference`` times the CPU oracle (the plain definition: fp64 scores
+and a full sort) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import signal
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "scored query-key pairs/s and ms per 8K-query chunk at 1M ctx, k=2048 (1 GB300)"
+UNIT = "pairs/s"
+FLOP_PER_PAIR = 2 * 64 * 128          # H * d multiply-adds per visible pair
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0                    # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+WORKLOADS = {
+    # name: (current chunk, previous chunk)
+    "1m": ("1m", "1m_prev"),
+    "256k": ("256k", "256k_prev"),
+    "128k": ("128k_chunk2", "128k_chunk1"),
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ltk", "reference"], default="ltk")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="1m")
+    ap.add_argument("--dtype", choices=["bf16", "fp8"], default="bf16")
+    ap.add_argument("--queries", type=int, default=0,
+                    help="run only the first N queries of the chunk (profiling a single wave)")
+    ap.add_argument("--cpu-queries", type=int, default=64,
+                    help="queries of the chunk the CPU oracle baseline scores")
+    ap.add_argument("--ref-queries", type=int, default=2,
+                    help="queries per step of the reference (oracle) arm")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decoupled", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ["indexer_topk_long_gb300/csrc/k_score_tc.cu", "indexer_topk_long_gb300/csrc/ltk_internal.cuh"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, dtype: str):
+    """DRAM bytes per filter-kernel launch from the committed ncu summary, if it
+    was captured on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"score_filter_{workload}_{dtype}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    hsh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not hsh or hsh.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.uuid = uuid
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def build_inputs(workload: str, dtype: str, seed: int, queries: int = 0):
+    """Host inputs of the current and previous chunk (shared key cache).
+    ``queries`` > 0 keeps only the first queries of each chunk."""
+    import dataclasses
+    from indexer_topk_long_gb300 import datagen
+    cur, prev = WORKLOADS[workload]
+    wl = datagen.WORKLOADS[cur]
+    wlp = datagen.WORKLOADS[prev]
+    if queries:
+        wl = dataclasses.replace(wl, T=min(queries, wl.T))
+        wlp = dataclasses.replace(wlp, T=min(queries, wlp.T))
+    keys = datagen.keys_fp32(wl.S, wl.d, seed)
+    inp = datagen.make_indexer_inputs(wl.T, wl.first_pos, wl.S, wl.H, wl.d, seed, dtype, keys=keys)
+    inp_prev = datagen.make_indexer_inputs(wlp.T, wlp.first_pos, wlp.S, wlp.H, wlp.d, seed, dtype,
+                                           keys=keys)
+    return wl, inp, inp_prev
+
+
+def to_dev(inp, torch, dev):
+    import numpy as np
+    if inp.dtype == "bf16":
+        q = torch.from_numpy(inp.q.view(np.int16)).to(dev)
+        k = torch.from_numpy(inp.k.view(np.int16)).to(dev)
+        qs = ks = None
+    else:
+        q = torch.from_numpy(inp.q).to(dev)
+        k = torch.from_numpy(inp.k).to(dev)
+        qs = torch.from_numpy(inp.q_scale).to(dev)
+        ks = torch.from_numpy(inp.k_scale).to(dev)
+    return dict(q=q, w=torch.from_numpy(inp.w).to(dev), k_cache=k,
+                positions=torch.from_numpy(inp.positions).to(dev), q_scale=qs, k_scale=ks)
+
+
+def cpu_oracle_rate(inp, k: int, n_queries: int):
+    """Oracle (plain fp64 definition + full sort) on a bounded sample of the
+    chunk's queries; returns (pairs/s, seconds, sample description)."""
+    import numpy as np
+    import oracle.indexer_topk as orc
+    keys64 = orc.widen_keys(inp)
+    T = inp.T
+    sel = sorted(set(np.linspace(0, T - 1, max(n_queries, 1)).astype(int).tolist()))
+    pairs = sum(orc.visible_count(inp.positions[t], inp.S, True) for t in sel)
+    t0 = time.perf_counter()
+    orc.indexer_topk(inp, k, queries=sel, keys64=keys64)
+    dt = time.perf_counter() - t0
+    return pairs / dt, dt, (f"{len(sel)} of {T} queries evenly spaced over the chunk "
+                            f"(first and last included), {pairs} visible pairs; key cache "
+                            f"widened to fp64 once before timing")
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, bounded sample per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle.indexer_topk as orc
+    wl, inp, _ = build_inputs(args.workload, args.dtype, 20260715)
+    keys64 = orc.widen_keys(inp)
+    T = inp.T
+    rng = np.random.default_rng(1)
+    def step():
+        sel = sorted(rng.choice(T, size=args.ref_queries, replace=False).tolist())
+        t0 = time.perf_counter()
+        orc.indexer_topk(inp, wl.k, queries=sel, keys64=keys64)
+        return sum(orc.visible_count(inp.positions[t], inp.S, True) for t in sel), time.perf_counter() - t0
+    for _ in range(args.warmup):
+        step()
+    pairs = secs = 0.0
+    for _ in range(args.steps):
+        p, s = step()
+        pairs += p
+        secs += s
+    value = pairs / secs
+    ms_per_chunk = wl.visible_pairs / value * 1e3
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_chunk,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded hot-key/topic generator)",
+        "config": {"workload": f"{args.workload} chunk, {args.dtype} inputs widened to fp64, k={wl.k}",
+                   "sample": f"{args.ref_queries} random queries of the chunk per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.ref_queries} queries per step x {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import numpy as np
+    import torch
+    from indexer_topk_long_gb300 import IndexerTopK
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    seed = 20260715 + rank        # each rank runs its own, independent chunk
+    wl, inp, inp_prev = build_inputs(args.workload, args.dtype, seed, args.queries)
+    d = to_dev(inp, torch, dev)
+    dp = to_dev(inp_prev, torch, dev)
+    k = wl.k
+    op = IndexerTopK(max_T=wl.T, max_S=wl.S, k=k, dtype=args.dtype,
+                     enable_decoupled=0, enable_host_io=0 if args.no_e2e else 1)
+    stream = torch.cuda.current_stream()
+
+    # previous chunk (its output provides the sample), outside the timed region
+    S_prev = inp_prev.S
+    prev_idx, _ = op(dp["q"], dp["w"], d["k_cache"][:S_prev], dp["positions"], k=k,
+                     q_scale=dp["q_scale"], k_scale=None if dp["k_scale"] is None else d["k_scale"][:S_prev])
+    out_idx = torch.empty((wl.T, k), dtype=torch.int32, device=dev)
+    out_score = torch.empty((wl.T, k), dtype=torch.float32, device=dev)
+
+    def step():
+        sample = op.make_sample(prev_idx, wl.S, 3 * k)
+        op(d["q"], d["w"], d["k_cache"], d["positions"], k=k, prev_topk=sample,
+           q_scale=d["q_scale"], k_scale=d["k_scale"], out=(out_idx, out_score))
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    warm = op.stats()
+    if warm["device_status"] != 0:
+        raise RuntimeError(f"device status {warm['device_status']}")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    launches0 = op.stats()["launches"]
+    op.set_timing(True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    st = op.stats()
+    op.set_timing(False)
+    launches = st["launches"] - launches0
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    pairs_step = st["visible_pairs"]
+    assert pairs_step == wl.visible_pairs, (pairs_step, wl.visible_pairs)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * pairs_step * args.steps / (elapsed_ms * 1e-3)
+
+    peaks, peaks_kind = measured_peaks()
+    bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak = bf16_peak * (FP8_OVER_BF16 if args.dtype == "fp8" else 1.0)
+    achieved = FLOP_PER_PAIR * pairs_step / (st["ms_filter"] * 1e-3) / 1e12
+    traffic = recorded_traffic(args.workload, args.dtype)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "score_tc_kernel<filter> (fused score + bin + gate + write-back)",
+                "peak_source": (f"{peaks_kind} bf16 sustained" +
+                                (" x 2 (nominal fp8/bf16 ratio)" if args.dtype == "fp8" else "")),
+                "algorithmic_flop_per_launch": FLOP_PER_PAIR * pairs_step}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+        "data": "synthetic (seeded hot-key/topic generator; no dataset)",
+        "config": {
+            "workload": (f"{args.workload} prefill chunk: T={wl.T} queries at positions "
+                         f"{wl.first_pos}..{wl.first_pos + wl.T - 1}, S={wl.S}, H={wl.H}, "
+                         f"d={wl.d}, k={k}, {args.dtype} q/k, fp32 w, previous-chunk top-3k sample"),
+            "l2": "inputs larger than L2 (key cache 256 MiB bf16 > 129 MB L2)",
+            "parallelism": f"replicas: {world} independent chunks, one per GPU",
+            "visible_pairs_per_chunk": pairs_step,
+        },
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "clocks": clock_info,
+        "stages_ms": {"sample": st["ms_sample"], "filter": st["ms_filter"],
+                      "select": st["ms_select"], "rescue": st["ms_rescue"],
+                      "total_fused_call": st["ms_total"]},
+        "candidates_per_query": st["cand_written"] / wl.T,
+        "candidates_max": st["cand_max"],
+        "n_overflow": st["n_overflow"],
+        "bytes_written_per_query": {"fused": 8.0 * st["cand_written"] / wl.T + 8.0 * k,
+                                    "decoupled": 4.0 * pairs_step / wl.T},
+    }
+
+    # ---- end to end through the host-buffer C-ABI call
+    if not args.no_e2e:
+        sample = op.make_sample(prev_idx, wl.S, 3 * k).cpu().pin_memory()
+        host = {key: (v.cpu().pin_memory() if v is not None else None) for key, v in d.items()}
+        hout = (torch.empty((wl.T, k), dtype=torch.int32, pin_memory=True),
+                torch.empty((wl.T, k), dtype=torch.float32, pin_memory=True))
+        def e2e_step():
+            op.topk_host(host["q"], host["w"], host["k_cache"], host["positions"], k=k,
+                         prev_topk=sample, q_scale=host["q_scale"], k_scale=host["k_scale"], out=hout)
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None) + \
+            sample.numel() * 4
+        d2h = sum(v.numel() * v.element_size() for v in hout)
+        line["e2e"] = {"value": world * pairs_step * args.steps / (e_ms * 1e-3), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e_ms / args.steps,
+                       "call": "ltk_indexer_topk_host (pinned host buffers, copies inside)"}
+        ok = torch.equal(hout[0], out_idx.cpu())
+        line["e2e"]["matches_device_call"] = bool(ok)
+        del host
+
+    # ---- same-GPU decoupled baseline (materialise fp32 scores, then select)
+    if not args.no_decoupled and world == 1:
+        dec = IndexerTopK(max_T=wl.T, max_S=wl.S, k=k, dtype=args.dtype, enable_decoupled=1)
+        di = torch.empty_like(out_idx)
+        ds = torch.empty_like(out_score)
+        def dec_step():
+            dec.decoupled(d["q"], d["w"], d["k_cache"], d["positions"], k=k, q_scale=d["q_scale"],
+                          k_scale=d["k_scale"], out=(di, ds))
+        dec_step()
+        torch.cuda.synchronize()
+        dec.set_timing(True)
+        n_dec = max(1, min(args.steps, 3))
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_dec):
+            dec_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        dst = dec.stats()
+        dec_ms = a0.elapsed_time(a1) / n_dec
+        line["decoupled"] = {"ms_per_step": dec_ms, "score_kernel_ms": dst["ms_filter"],
+                             "select_ms": dst["ms_select"],
+                             "score_matrix_bytes": 4 * wl.T * wl.S,
+                             "fused_speedup": dec_ms / ms_per_step,
+                             "identical_output": bool(torch.equal(di, out_idx) and torch.equal(ds, out_score))}
+        dec.close()
+        del dec
+        torch.cuda.empty_cache()
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    if not args.no_cpu and world == 1 and rank == 0:
+        rate, secs, desc = cpu_oracle_rate(inp, k, args.cpu_queries)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": desc, "seconds": secs}
+
+    op.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

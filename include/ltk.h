@@ -113,8 +113,12 @@ typedef struct ltk_handle ltk_handle;
  *   cand_max       largest per-query candidate count.
  *   n_overflow     queries whose list exceeded cand_cap (recomputed exactly).
  *   device_status  first error code raised on the device, 0 if none.
- *   ms_*           stage times (CUDA events on the call's stream) when timing
- *                  is enabled with ltk_set_timing, else -1.
+ *   visible_pairs  query-key pairs the last call scored (sum of V_t).
+ *   ms_*           stage times from CUDA events recorded on each call's
+ *                  stream while timing is enabled (ltk_set_timing), averaged
+ *                  over the last timed_calls calls (at most 64) since timing
+ *                  was last enabled; -1 when no call was timed.
+ *   launches       kernels this library launched in the process so far.
  */
 typedef struct {
   int T;
@@ -130,6 +134,8 @@ typedef struct {
   float ms_select;
   float ms_rescue;
   float ms_total;
+  int timed_calls;
+  long long launches;
 } ltk_stats;
 
 /* ABI version of the loaded library (LTK_ABI_VERSION). */
@@ -155,7 +161,8 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out);
  * NULL is accepted. */
 void ltk_destroy(ltk_handle* h);
 
-/* Enables (1) or disables (0) per-stage CUDA-event timing on later calls. */
+/* Enables (1) or disables (0) per-stage CUDA-event timing on later calls;
+ * enabling also restarts the averaging window of ltk_get_stats. */
 ltk_status ltk_set_timing(ltk_handle* h, int enable);
 
 /*

@@ -321,6 +321,7 @@ cudaError_t launch_random_sample(long long S, int n, unsigned long long seed, in
                                  cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   random_sample_kernel<<<(n + 255) / 256, 256, 0, stream>>>(S, n, seed, out);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -338,6 +339,7 @@ cudaError_t launch_prepare_sample(const int* ids, int n, long long S, int n_pad,
     configured = true;
   }
   prepare_sample_kernel<<<1, kPrepThreads, smem, stream>>>(ids, n, S, n_pad, key_ids_pad);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -351,6 +353,7 @@ cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int el
   gather_keys_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(k_cache), k_scale, vec,
                                                  key_ids_pad, n_pad, static_cast<uint4*>(k_samp),
                                                  k_scale_samp);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -366,6 +369,7 @@ cudaError_t launch_sample_stats(const SampleStatsParams& p, cudaStream_t stream)
     configured = true;
   }
   sample_stats_kernel<<<p.T, kStatsThreads, smem, stream>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -384,6 +388,7 @@ cudaError_t launch_make_sample(const int* prev_idx, long long n_prev, long long 
     digit_pick_kernel<<<1, 32, 0, stream>>>(ws.hist, shift, ws.state);
   }
   collect_top_kernel<<<grid_for(S, 256, 4096), 256, 0, stream>>>(ws.keys, S, ws.state, n, out);
+  count_launches((n_prev > 0 ? 1 : 0) + 3 + 2 * 8);
   return cudaGetLastError();
 }
 

@@ -18,7 +18,8 @@
 //     weighted head sum is intra-thread.  TMEM (512 columns) holds two
 //     accumulators, one per half of the query block; the epilogue drains one
 //     half while the tensor core fills the other.
-//   * Epilogue (8 warps): tcgen05.ld -> ReLU, w-weighted head sum (fp32 FMA)
+//   * Epilogue (8 warps): tcgen05.ld (16x256b) -> ReLU, w-weighted head sum
+//     with the weights in registers (packed fp32x2 FMA, quad reduce-scatter)
 //     -> mask -> [dense: store I] or [filter: bin, gate, warp ballot append,
 //     shared-memory histogram].
 //   * Warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warp 2 =
@@ -79,18 +80,49 @@ constexpr size_t smem_bytes(int nb) {
          static_cast<size_t>(kTcQPB) * nb * sizeof(int);
 }
 
-// sum_h w[h] * max(0, v[h]) in fp32, fixed order (4 interleaved partial sums).
-__device__ __forceinline__ float head_sum(const float* v, const float* w) {
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+// One query's weighted head sum for the 32 keys of a warp's TMEM lane quarter.
+// The warp reads the query's 64 accumulator columns with two 16x256b loads
+// (lanes 0-15 and 16-31 of the quarter): thread t (c = t % 4) then holds 16
+// heads {8r + 2c + i} of the 4 keys t/4 + {0, 8, 16, 24}.  head_partials forms
+// the 4 partial sums sum_h w[h] * max(0, x[h]) over those heads with packed
+// fp32x2 FMAs (the 16 weights held in registers); quad_reduce then leaves
+// thread t with the full sum of key t/4 + 8c.
+struct Partials {
+  float p0, p1, p2, p3;   // keys t/4 + {0, 8, 16, 24}, this thread's 16 heads
+};
+
+__device__ __forceinline__ Partials head_partials(uint32_t taddr, const float (&w)[16],
+                                                  float after = 0.f) {
+  float va[32], vb[32];
+  tmem_ld16x256b_x8(taddr, va, after);
+  tmem_ld16x256b_x8(taddr + (16u << 16), vb, after);
+  tmem_wait_ld();
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
 #pragma unroll
-  for (int h = 0; h < kTcHeads; h += 4) {
-    const float4 wv = *reinterpret_cast<const float4*>(w + h);
-    a0 = __fmaf_rn(fmaxf(v[h + 0], 0.f), wv.x, a0);
-    a1 = __fmaf_rn(fmaxf(v[h + 1], 0.f), wv.y, a1);
-    a2 = __fmaf_rn(fmaxf(v[h + 2], 0.f), wv.z, a2);
-    a3 = __fmaf_rn(fmaxf(v[h + 3], 0.f), wv.w, a3);
+  for (int r = 0; r < 8; ++r) {
+    const float2 w0 = make_float2(w[2 * r], w[2 * r]);
+    const float2 w1 = make_float2(w[2 * r + 1], w[2 * r + 1]);
+    ffma2(a0, make_float2(fmaxf(va[4 * r + 0], 0.f), fmaxf(va[4 * r + 2], 0.f)), w0);
+    ffma2(a1, make_float2(fmaxf(va[4 * r + 1], 0.f), fmaxf(va[4 * r + 3], 0.f)), w1);
+    ffma2(b0, make_float2(fmaxf(vb[4 * r + 0], 0.f), fmaxf(vb[4 * r + 2], 0.f)), w0);
+    ffma2(b1, make_float2(fmaxf(vb[4 * r + 1], 0.f), fmaxf(vb[4 * r + 3], 0.f)), w1);
   }
-  return __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3));
+  return Partials{__fadd_rn(a0.x, a1.x), __fadd_rn(a0.y, a1.y), __fadd_rn(b0.x, b1.x),
+                  __fadd_rn(b0.y, b1.y)};
+}
+
+// Reduce-scatter over the quad: keep keys {c&2, (c&2)+1}, then key c.
+__device__ __forceinline__ float quad_reduce(const Partials& q, int c) {
+  const float p0 = q.p0, p1 = q.p1, p2 = q.p2, p3 = q.p3;
+  const bool hi = (c & 2) != 0;
+  float k0 = hi ? p2 : p0, k1 = hi ? p3 : p1;
+  const float s0 = hi ? p0 : p2, s1 = hi ? p1 : p3;
+  k0 = __fadd_rn(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 2));
+  k1 = __fadd_rn(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 2));
+  const bool odd = (c & 1) != 0;
+  const float keep = odd ? k1 : k0;
+  const float send = odd ? k0 : k1;
+  return __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1));
 }
 
 // Threshold refresh by one warp (Methodology step 2, "Threshold Refresh"):
@@ -98,34 +130,28 @@ __device__ __forceinline__ float head_sum(const float* v, const float* w) {
 // whose cumulative count reaches k.  Counts only grow and each counted key is
 // distinct, so any b found is a valid lower bound on the bin of the true k-th
 // score; the store is a plain overwrite, never below the current value.
+// The scan walks 32-bin segments from the top (lane l reads bin top-1-l, so a
+// segment is one conflict-free shared-memory access) and stops at the segment
+// holding the current threshold: bins below it cannot raise it.
 __device__ __forceinline__ void refresh_threshold(const int* hist, int nb, int k,
                                                   volatile int* theta, int lane) {
   const volatile int* hv = hist;
-  const int per = nb >> 5;
-  const int hi = nb - lane * per;
-  const int lo = hi - per;
-  int seg = 0;
-  for (int b = lo; b < hi; ++b) seg += hv[b];
-  int cum = seg;
+  const int cur = *theta;
+  int run = 0;
+  for (int top = nb; top > cur; top -= 32) {
+    int cum = hv[top - 1 - lane];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xFFFFFFFFu, cum, o);
-    if (lane >= o) cum += n;
-  }
-  const unsigned m = __ballot_sync(0xFFFFFFFFu, cum >= k);
-  if (m == 0) return;
-  const int L = __ffs(m) - 1;
-  if (lane == L) {
-    int run = cum - seg;
-    int th = lo;
-    for (int b = hi - 1; b >= lo; --b) {
-      run += hv[b];
-      if (run >= k) {
-        th = b;
-        break;
-      }
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+      if (lane >= o) cum += n;
     }
-    if (th > *theta) *theta = th;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, run + cum >= k);
+    if (m != 0) {
+      const int th = top - 1 - (__ffs(m) - 1);
+      if (lane == 0 && th > cur) *theta = th;
+      return;
+    }
+    run += __shfl_sync(0xFFFFFFFFu, cum, 31);
   }
 }
 
@@ -162,11 +188,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = static_cast<int>((last_row + kTile - 1) / kTile);
 
   // ---- setup: weights, per-query state, histogram, barriers, TMEM
+  // Weights in the epilogue's order: entry [ql][c][2r + i] holds head
+  // 8r + 2c + i, so quad thread c reads its 16 weights as 4 float4 loads.
   for (int i = tid; i < kTcQPB * kTcHeads; i += kThreads) {
     const int ql = i / kTcHeads;
+    const int c = (i % kTcHeads) / 16;
+    const int r = (i % 16) / 2;
+    const int h = 8 * r + 2 * c + (i & 1);
     float wv = 0.f;
     if (ql < nq) {
-      wv = p.w[static_cast<size_t>(t0 + ql) * kTcHeads + (i % kTcHeads)];
+      wv = p.w[static_cast<size_t>(t0 + ql) * kTcHeads + h];
       if constexpr (FP8) wv = __fmul_rn(wv, p.q_scale[t0 + ql]);
     }
     w_s[i] = wv;
@@ -315,8 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- epilogue ----------------
       const int e = warp - kEpiWarp0;
       const int lq = warp & 3;               // TMEM lane quarter this warp may access
-      const int qp = e >> 2;                 // which query pair of a half
-      const int row = lq * 32 + lane;
+      const int qp = e >> 2;                 // which query pair of each half
+      const int c = lane & 3;
+      const int row = lq * 32 + (lane >> 2) + 8 * c;   // key row this thread finishes
       const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
       for (int i = 0; i < n_tiles; ++i) {
         const long long key = static_cast<long long>(i) * kTile + row;
@@ -326,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kid = static_cast<int>(key);
         if (MODE == kModeDense && p.key_ids != nullptr) kid = key_ok ? p.key_ids[key] : INT_MAX;
         bool stop = false;
-        for (int j = 0; j < 2 && !stop; ++j) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
           bool ok = mbar_wait(smem_u32(&ctrl->acc_full[j]), i & 1, abort_flag, p.status);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) {
@@ -334,21 +367,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-#pragma unroll 1
+          // Read both queries' accumulators, then hand the TMEM half back to
+          // the MMA warp before the gate and write-back work.
+          // this thread's 16 weights of each of the two queries
+          float wr[2][16];
+#pragma unroll
+          for (int qq = 0; qq < 2; ++qq) {
+            const float4* src =
+                reinterpret_cast<const float4*>(w_s + (j * 4 + qp * 2 + qq) * kTcHeads + c * 16);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const float4 x = src[v4];
+              wr[qq][4 * v4 + 0] = x.x;
+              wr[qq][4 * v4 + 1] = x.y;
+              wr[qq][4 * v4 + 2] = x.z;
+              wr[qq][4 * v4 + 3] = x.w;
+            }
+          }
+          const uint32_t tq = tmem + lane_base + j * kN + (qp * 2) * kTcHeads;
+          const Partials part0 = head_partials(tq, wr[0]);
+          const Partials part1 = head_partials(tq + kTcHeads, wr[1], part0.p3);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[j]));
+#pragma unroll
           for (int qq = 0; qq < 2; ++qq) {
             const int qh = qp * 2 + qq;         // query within the half
             const int ql = j * 4 + qh;          // query within the CTA
-            float v[kTcHeads];
-            const uint32_t ta = tmem + lane_base + j * kN + qh * kTcHeads;
-            tmem_ld32(ta, v);
-            tmem_ld32(ta + 32, v + 32);
-            tmem_wait_ld();
-            if (qq == 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[j]));
-            }
-            float I = head_sum(v, w_s + ql * kTcHeads);
+            float I = quad_reduce(qq == 0 ? part0 : part1, c);
             if constexpr (FP8) I = __fmul_rn(I, kscale);
             if constexpr (MODE == kModeDense) {
               if (ql < nq && key_ok) {
@@ -412,6 +458,7 @@ cudaError_t launch_one(const CUtensorMap& qm, const CUtensorMap& km, const Score
     configured = smem_bytes<FP8>(Shape<FP8>::kMaxBins);
   }
   score_tc_kernel<MODE, FP8><<<grid, kThreads, smem, stream>>>(qm, km, p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

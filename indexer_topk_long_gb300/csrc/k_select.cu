@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   const int t = blockIdx.x;
   const int V = visible_of(p.positions, t, p.S, p.causal);
   const int kk = min(p.k, V);
+  if (threadIdx.x == 0 && p.pairs != nullptr) atomicAdd(p.pairs, static_cast<unsigned long long>(V));
   const int n_raw = p.cnt[t];
   if (n_raw > p.cap) {
     if (threadIdx.x == 0) {
@@ -420,6 +421,7 @@ __global__ void __launch_bounds__(kSelThreads) row_topk_kernel(const RowTopkPara
   const int t = blockIdx.x;
   const int V = visible_of(p.positions, t, p.S, p.causal);
   const int kk = min(p.k, V);
+  if (threadIdx.x == 0 && p.pairs != nullptr) atomicAdd(p.pairs, static_cast<unsigned long long>(V));
   row_topk_block(p.rows + static_cast<size_t>(t) * p.ld, V, kk, p.k, t, p.out_idx, p.out_score,
                  rt_smem, hist256, sh, sh_int);
 }
@@ -549,6 +551,7 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
     configured = true;
   }
   select_kernel<<<p.T, kSelThreads, smem, stream>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -563,6 +566,7 @@ cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream) {
     configured = true;
   }
   row_topk_kernel<<<p.T, kSelThreads, smem, stream>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -579,6 +583,7 @@ cudaError_t launch_rescue(const RescueParams& p, int rescue_rows, cudaStream_t s
     configured = true;
   }
   rescue_kernel<<<rescue_rows, kRescueThreads, smem, stream>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -7,6 +7,7 @@
 // steps 1-3 (Sample, Filter, Select).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -50,18 +51,28 @@ struct ltk_handle {
   int* io_prev = nullptr;
   int* io_oidx = nullptr;
   float* io_oscore = nullptr;
-  // timing
-  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  // timing: a ring of per-call stage events (5 per call)
+  static constexpr int kRing = 64;
+  cudaEvent_t ring[kRing][5] = {};
   int timing = 0;
-  int timed_last = 0;
+  int ring_calls = 0;                  // timed calls since timing was enabled
+  cudaEvent_t* ev = nullptr;           // events of the current call (or null)
+  unsigned long long* pairs = nullptr; // [1] visible pairs of the last call
   int last_kind = 0;                   // 0 none, 1 fused, 2 decoupled
   // last call
   int last_T = 0;
   long long last_S = 0;
   int last_k = 0;
-  long long last_pairs = 0;
   cudaStream_t last_stream = nullptr;
 };
+
+namespace ltk {
+namespace {
+std::atomic<long long> g_launches{0};
+}
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+long long launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
+}  // namespace ltk
 
 namespace {
 
@@ -192,8 +203,18 @@ void free_all(ltk_handle* h) {
                   h->io_oidx,     h->io_oscore};
   for (void* p : ptrs)
     if (p) cudaFree(p);
-  for (auto& e : h->ev)
-    if (e) cudaEventDestroy(e);
+  if (h->pairs) cudaFree(h->pairs);
+  for (auto& row : h->ring)
+    for (auto& e : row)
+      if (e) cudaEventDestroy(e);
+}
+
+// Events of this call's stages, or null when timing is off.
+cudaEvent_t* begin_timed_call(ltk_handle* h) {
+  if (!h->timing) return nullptr;
+  cudaEvent_t* ev = h->ring[h->ring_calls % ltk_handle::kRing];
+  ++h->ring_calls;
+  return ev;
 }
 
 bool current_device_is(int dev) {
@@ -234,11 +255,6 @@ ltk_status validate_call(const ltk_handle* h, const CallArgs& a) {
   return LTK_OK;
 }
 
-long long visible_pairs_estimate(const ltk_handle* h, int T, long long S) {
-  (void)h;
-  return static_cast<long long>(T) * S;   // refined from positions in ltk_get_stats
-}
-
 ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int n_prev,
                      cudaStream_t st) {
   const ltk_config& c = h->cfg;
@@ -248,11 +264,11 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   h->last_S = a.S;
   h->last_k = a.k;
   h->last_stream = st;
-  h->last_pairs = visible_pairs_estimate(h, a.T, a.S);
-  h->timed_last = h->timing;
   if (a.T == 0) return LTK_OK;
-  if (h->timing) LTK_CUDA(cudaEventRecord(h->ev[0], st));
+  h->ev = begin_timed_call(h);
+  if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[0], st));
   LTK_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), st));
+  LTK_CUDA(cudaMemsetAsync(h->pairs, 0, sizeof(unsigned long long), st));
   LTK_CUDA(cudaMemsetAsync(h->ovf, 0, 2 * sizeof(int), st));
 
   // ---- Sample (Methodology step 1)
@@ -291,7 +307,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   LTK_CUDA(launch_score_tc(kModeDense, fp8, q_map, ks_map, sp, st));
   SampleStatsParams stp{h->samp_scores, n_pad, n_pad, a.T, a.k, c.n_bins, h->s_min, h->delta, h->theta0};
   LTK_CUDA(launch_sample_stats(stp, st));
-  if (h->timing) LTK_CUDA(cudaEventRecord(h->ev[1], st));
+  if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
 
   // ---- Filter (Methodology step 2)
   ScoreParams fp{};
@@ -314,13 +330,13 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   fp.refresh_interval = c.refresh_interval;
   fp.status = h->status;
   LTK_CUDA(launch_score_tc(kModeFilter, fp8, q_map, k_map, fp, st));
-  if (h->timing) LTK_CUDA(cudaEventRecord(h->ev[2], st));
+  if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[2], st));
 
   // ---- Select (Methodology step 3)
   SelectParams sel{h->cand, h->cnt, c.causal ? a.positions : nullptr, a.T, a.S, c.causal, h->cap,
-                   a.k, a.out_idx, a.out_score, h->ovf, h->ovf + 2};
+                   a.k, a.out_idx, a.out_score, h->ovf, h->ovf + 2, h->pairs};
   LTK_CUDA(launch_select(sel, st));
-  if (h->timing) LTK_CUDA(cudaEventRecord(h->ev[3], st));
+  if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[3], st));
 
   // ---- exact rescue of overflowed candidate lists (no-op when none)
   RescueParams rp{};
@@ -346,7 +362,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   rp.out_idx = a.out_idx;
   rp.out_score = a.out_score;
   LTK_CUDA(launch_rescue(rp, h->rescue_rows, st));
-  if (h->timing) LTK_CUDA(cudaEventRecord(h->ev[4], st));
+  if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[4], st));
   return LTK_OK;
 }
 
@@ -448,7 +464,9 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
     step(alloc(&h->io_oidx, T * cfg->k * 4ull));
     step(alloc(&h->io_oscore, T * cfg->k * 4ull));
   }
-  for (auto& ev : h->ev) step(cudaEventCreate(&ev));
+  step(alloc(&h->pairs, 8));
+  for (auto& row : h->ring)
+    for (auto& ev : row) step(cudaEventCreate(&ev));
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->ovf, 0, 8);
   if (e == cudaSuccess) e = cudaMemset(h->cnt, 0, T * 4);
@@ -471,6 +489,7 @@ void ltk_destroy(ltk_handle* h) {
 ltk_status ltk_set_timing(ltk_handle* h, int enable) {
   if (h == nullptr) return LTK_ERR_ARG;
   h->timing = enable ? 1 : 0;
+  h->ring_calls = 0;
   return LTK_OK;
 }
 
@@ -562,10 +581,11 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   h->last_S = S;
   h->last_k = k;
   h->last_stream = st;
-  h->timed_last = h->timing;
   if (T == 0) return LTK_OK;
-  if (h->timing) LTK_CUDA(cudaEventRecord(h->ev[0], st));
+  h->ev = begin_timed_call(h);
+  if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[0], st));
   LTK_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), st));
+  LTK_CUDA(cudaMemsetAsync(h->pairs, 0, sizeof(unsigned long long), st));
   LTK_CUDA(cudaMemsetAsync(h->ovf, 0, 2 * sizeof(int), st));
   CUtensorMap q_map, k_map;
   if (!make_tmap(&q_map, q, fp8, c.dim, static_cast<unsigned long long>(T) * c.heads, 256) ||
@@ -583,12 +603,13 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   sp.dense = h->dense;
   sp.ld = S;
   sp.status = h->status;
-  if (h->timing) LTK_CUDA(cudaEventRecord(h->ev[1], st));
+  if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
   LTK_CUDA(launch_score_tc(kModeDense, fp8, q_map, k_map, sp, st));
-  if (h->timing) LTK_CUDA(cudaEventRecord(h->ev[2], st));
-  RowTopkParams rp{h->dense, S, c.causal ? positions : nullptr, T, S, c.causal, k, out_idx, out_score};
+  if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[2], st));
+  RowTopkParams rp{h->dense, S, c.causal ? positions : nullptr, T, S, c.causal, k, out_idx, out_score,
+                   h->pairs};
   LTK_CUDA(launch_row_topk(rp, st));
-  if (h->timing) {
+  if (h->ev) {
     LTK_CUDA(cudaEventRecord(h->ev[3], st));
     LTK_CUDA(cudaEventRecord(h->ev[4], st));
   }
@@ -628,14 +649,29 @@ ltk_status ltk_get_stats(ltk_handle* h, ltk_stats* out) {
     LTK_CUDA(cudaMemcpy(&ovf, h->ovf, 4, cudaMemcpyDeviceToHost));
     out->n_overflow = ovf;
   }
-  out->visible_pairs = h->last_pairs;
-  if (h->timed_last) {
-    float ms = 0.f;
-    if (cudaEventElapsedTime(&ms, h->ev[0], h->ev[1]) == cudaSuccess) out->ms_sample = ms;
-    if (cudaEventElapsedTime(&ms, h->ev[1], h->ev[2]) == cudaSuccess) out->ms_filter = ms;
-    if (cudaEventElapsedTime(&ms, h->ev[2], h->ev[3]) == cudaSuccess) out->ms_select = ms;
-    if (cudaEventElapsedTime(&ms, h->ev[3], h->ev[4]) == cudaSuccess) out->ms_rescue = ms;
-    if (cudaEventElapsedTime(&ms, h->ev[0], h->ev[4]) == cudaSuccess) out->ms_total = ms;
+  if (h->last_T > 0) {
+    unsigned long long pairs = 0;
+    LTK_CUDA(cudaMemcpy(&pairs, h->pairs, 8, cudaMemcpyDeviceToHost));
+    out->visible_pairs = static_cast<long long>(pairs);
+  }
+  out->launches = launches_so_far();
+  const int n = h->ring_calls < ltk_handle::kRing ? h->ring_calls : ltk_handle::kRing;
+  if (n > 0) {
+    double acc[5] = {0, 0, 0, 0, 0};
+    const int pairs_of[5][2] = {{0, 1}, {1, 2}, {2, 3}, {3, 4}, {0, 4}};
+    for (int i = 0; i < n; ++i) {
+      for (int j = 0; j < 5; ++j) {
+        float ms = 0.f;
+        LTK_CUDA(cudaEventElapsedTime(&ms, h->ring[i][pairs_of[j][0]], h->ring[i][pairs_of[j][1]]));
+        acc[j] += ms;
+      }
+    }
+    out->ms_sample = static_cast<float>(acc[0] / n);
+    out->ms_filter = static_cast<float>(acc[1] / n);
+    out->ms_select = static_cast<float>(acc[2] / n);
+    out->ms_rescue = static_cast<float>(acc[3] / n);
+    out->ms_total = static_cast<float>(acc[4] / n);
+    out->timed_calls = n;
   }
   return LTK_OK;
 }

@@ -229,6 +229,38 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// tcgen05.ld 16x256b, 8 repetitions along columns (64 fp32 columns of 16
+// lanes).  Fragment layout (PTX ISA, tcgen05 matrix fragments, shape
+// 16x256b): in repetition r, thread t holds columns 8r + 2(t%4) + {0,1} of lane
+// t/4 in registers 4r+{0,1} and of lane t/4 + 8 in registers 4r+{2,3}.
+// `after` is not used by the instruction: passing a value computed from an
+// earlier load makes this load wait for that computation, which bounds how
+// many loaded registers are live at once.
+__device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, float* v, float after = 0.f) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr), "f"(after));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Packed fp32x2 fused multiply-add (sm_100+): acc = a * b + acc, lane-wise.
+__device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
+  unsigned long long A, B, C;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(acc.x), "f"(acc.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(C) : "l"(A), "l"(B));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(C));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -263,6 +295,10 @@ __host__ __device__ constexpr uint32_t make_idesc(bool fp8, int M, int N) {
 // ---------------------------------------------------------------------------
 // Kernel parameter blocks and launch functions (defined in the kernel files)
 // ---------------------------------------------------------------------------
+// Process-wide count of kernels launched by this library (ltk_api.cu).
+void count_launches(int n);
+long long launches_so_far();
+
 enum ScoreMode { kModeDense = 0, kModeFilter = 1 };
 
 struct ScoreParams {
@@ -342,6 +378,7 @@ struct SelectParams {
   float* out_score;                // [T, k]
   int* ovf_count;
   int* ovf_list;                   // [T]
+  unsigned long long* pairs;       // visible pairs of the call (accumulated)
 };
 
 struct RowTopkParams {
@@ -354,6 +391,7 @@ struct RowTopkParams {
   int k;
   int* out_idx;
   float* out_score;
+  unsigned long long* pairs;       // visible pairs of the call (accumulated)
 };
 
 struct RescueParams {

@@ -42,7 +42,8 @@ class Stats(ctypes.Structure):
                 ("cand_max", ctypes.c_int), ("n_overflow", ctypes.c_int),
                 ("device_status", ctypes.c_int), ("ms_sample", ctypes.c_float),
                 ("ms_filter", ctypes.c_float), ("ms_select", ctypes.c_float),
-                ("ms_rescue", ctypes.c_float), ("ms_total", ctypes.c_float)]
+                ("ms_rescue", ctypes.c_float), ("ms_total", ctypes.c_float),
+                ("timed_calls", ctypes.c_int), ("launches", ctypes.c_longlong)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
