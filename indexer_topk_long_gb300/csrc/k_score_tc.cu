@@ -18,12 +18,14 @@
 //     weighted head sum is intra-thread.  TMEM (512 columns) holds two
 //     accumulators, one per half of the query block; the epilogue drains one
 //     half while the tensor core fills the other.
-//   * Epilogue (8 warps): tcgen05.ld (16x256b) -> ReLU, w-weighted head sum
-//     with the weights in registers (packed fp32x2 FMA, quad reduce-scatter)
-//     -> mask -> [dense: store I] or [filter: bin, gate, warp ballot append,
+//   * Epilogue (16 warps, one per TMEM lane quarter and query of a half):
+//     tcgen05.ld (16x256b) of the query's 64 columns, release of the TMEM half
+//     right after the load, then ReLU and the w-weighted head sum with the
+//     weights in registers (packed fp32x2 FMA, quad reduce-scatter) -> mask ->
+//     [dense: store I] or [filter: bin, gate, warp ballot append,
 //     shared-memory histogram].
 //   * Warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warp 2 =
-//     threshold refresh, warp 3 idle.
+//     threshold refresh.
 // Every wait is bounded (2 s); on expiry the kernel records LTK_ERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <climits>
@@ -47,9 +49,9 @@ struct Shape {
   static constexpr int kBoxCols = FP8 ? 128 : 64;             // elements per 128-byte box row
 };
 
-constexpr int kThreads = 384;
-constexpr int kEpiWarp0 = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarp0 = 3;
+constexpr int kEpiWarps = 16;           // 4 per TMEM lane quarter, one query per half each
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kRefreshWarp = 2;
 constexpr int kN = 256;                 // MMA N: 4 queries x 64 heads
 constexpr uint32_t kTmemCols = 512;
@@ -80,40 +82,31 @@ constexpr size_t smem_bytes(int nb) {
          static_cast<size_t>(kTcQPB) * nb * sizeof(int);
 }
 
-// One query's weighted head sum for the 32 keys of a warp's TMEM lane quarter.
-// The warp reads the query's 64 accumulator columns with two 16x256b loads
-// (lanes 0-15 and 16-31 of the quarter): thread t (c = t % 4) then holds 16
-// heads {8r + 2c + i} of the 4 keys t/4 + {0, 8, 16, 24}.  head_partials forms
-// the 4 partial sums sum_h w[h] * max(0, x[h]) over those heads with packed
-// fp32x2 FMAs (the 16 weights held in registers); quad_reduce then leaves
-// thread t with the full sum of key t/4 + 8c.
-struct Partials {
-  float p0, p1, p2, p3;   // keys t/4 + {0, 8, 16, 24}, this thread's 16 heads
-};
-
-__device__ __forceinline__ Partials head_partials(uint32_t taddr, const float (&w)[16],
-                                                  float after = 0.f) {
-  float va[32], vb[32];
-  tmem_ld16x256b_x8(taddr, va, after);
-  tmem_ld16x256b_x8(taddr + (16u << 16), vb, after);
-  tmem_wait_ld();
-  float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
+// One query's weighted head sum for the 32 keys of a warp's TMEM lane quarter:
+// the warp reads the query's 64 accumulator columns with two 16x256b loads
+// (lanes 0-15 and 16-31 of the quarter), so thread t (c = t % 4) holds 16
+// heads {8r + 2c + i} of the 4 keys t/4 + {0, 8, 16, 24}.
+//
+// Partial weighted head sums of one query for 2 keys: va holds a 16x256b x8
+// load (64 columns of 16 lanes), so thread t (c = t % 4) has heads
+// {8r + 2c + i} of keys t/4 and t/4 + 8; w holds the weights of those heads.
+// Returns the two partial sums sum_h w[h] * max(0, x[h]) (packed fp32x2 FMA).
+__device__ __forceinline__ float2 head_partials(const float* va, const float (&w)[16]) {
+  float2 a0 = make_float2(0.f, 0.f), a1 = a0;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    const float2 w0 = make_float2(w[2 * r], w[2 * r]);
-    const float2 w1 = make_float2(w[2 * r + 1], w[2 * r + 1]);
-    ffma2(a0, make_float2(fmaxf(va[4 * r + 0], 0.f), fmaxf(va[4 * r + 2], 0.f)), w0);
-    ffma2(a1, make_float2(fmaxf(va[4 * r + 1], 0.f), fmaxf(va[4 * r + 3], 0.f)), w1);
-    ffma2(b0, make_float2(fmaxf(vb[4 * r + 0], 0.f), fmaxf(vb[4 * r + 2], 0.f)), w0);
-    ffma2(b1, make_float2(fmaxf(vb[4 * r + 1], 0.f), fmaxf(vb[4 * r + 3], 0.f)), w1);
+    ffma2(a0, make_float2(fmaxf(va[4 * r + 0], 0.f), fmaxf(va[4 * r + 2], 0.f)),
+          make_float2(w[2 * r], w[2 * r]));
+    ffma2(a1, make_float2(fmaxf(va[4 * r + 1], 0.f), fmaxf(va[4 * r + 3], 0.f)),
+          make_float2(w[2 * r + 1], w[2 * r + 1]));
   }
-  return Partials{__fadd_rn(a0.x, a1.x), __fadd_rn(a0.y, a1.y), __fadd_rn(b0.x, b1.x),
-                  __fadd_rn(b0.y, b1.y)};
+  return make_float2(__fadd_rn(a0.x, a1.x), __fadd_rn(a0.y, a1.y));
 }
 
-// Reduce-scatter over the quad: keep keys {c&2, (c&2)+1}, then key c.
-__device__ __forceinline__ float quad_reduce(const Partials& q, int c) {
-  const float p0 = q.p0, p1 = q.p1, p2 = q.p2, p3 = q.p3;
+// Reduce-scatter over the quad of threads that hold the same 4 keys
+// t/4 + {0, 8, 16, 24} (partials p0..p3 over different heads): keep keys
+// {c&2, (c&2)+1}, then key c.  Thread t ends with the full sum of key t/4 + 8c.
+__device__ __forceinline__ float quad_reduce(float p0, float p1, float p2, float p3, int c) {
   const bool hi = (c & 2) != 0;
   float k0 = hi ? p2 : p0, k1 = hi ? p3 : p1;
   const float s0 = hi ? p0 : p2, s1 = hi ? p1 : p3;
@@ -346,10 +339,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- epilogue ----------------
       const int e = warp - kEpiWarp0;
       const int lq = warp & 3;               // TMEM lane quarter this warp may access
-      const int qp = e >> 2;                 // which query pair of each half
+      const int qh = e >> 2;                 // this warp's query within each half
       const int c = lane & 3;
       const int row = lq * 32 + (lane >> 2) + 8 * c;   // key row this thread finishes
       const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
+      // weights of this thread's 16 heads {8r + 2c + i} for query qh of each half
+      float wr[2][16];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float4* src = reinterpret_cast<const float4*>(w_s + (j * 4 + qh) * kTcHeads + c * 16);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          const float4 x = src[v4];
+          wr[j][4 * v4 + 0] = x.x;
+          wr[j][4 * v4 + 1] = x.y;
+          wr[j][4 * v4 + 2] = x.z;
+          wr[j][4 * v4 + 3] = x.w;
+        }
+      }
       for (int i = 0; i < n_tiles; ++i) {
         const long long key = static_cast<long long>(i) * kTile + row;
         const bool key_ok = key < p.rows;
@@ -367,59 +374,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // Read both queries' accumulators, then hand the TMEM half back to
-          // the MMA warp before the gate and write-back work.
-          // this thread's 16 weights of each of the two queries
-          float wr[2][16];
-#pragma unroll
-          for (int qq = 0; qq < 2; ++qq) {
-            const float4* src =
-                reinterpret_cast<const float4*>(w_s + (j * 4 + qp * 2 + qq) * kTcHeads + c * 16);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              const float4 x = src[v4];
-              wr[qq][4 * v4 + 0] = x.x;
-              wr[qq][4 * v4 + 1] = x.y;
-              wr[qq][4 * v4 + 2] = x.z;
-              wr[qq][4 * v4 + 3] = x.w;
-            }
-          }
-          const uint32_t tq = tmem + lane_base + j * kN + (qp * 2) * kTcHeads;
-          const Partials part0 = head_partials(tq, wr[0]);
-          const Partials part1 = head_partials(tq + kTcHeads, wr[1], part0.p3);
+          // read the query's 64 columns, then hand the TMEM half back at once
+          const uint32_t ta = tmem + lane_base + j * kN + qh * kTcHeads;
+          float va[32], vb[32];
+          tmem_ld16x256b_x8(ta, va);
+          tmem_ld16x256b_x8(ta + (16u << 16), vb);
+          tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[j]));
-#pragma unroll
-          for (int qq = 0; qq < 2; ++qq) {
-            const int qh = qp * 2 + qq;         // query within the half
-            const int ql = j * 4 + qh;          // query within the CTA
-            float I = quad_reduce(qq == 0 ? part0 : part1, c);
-            if constexpr (FP8) I = __fmul_rn(I, kscale);
-            if constexpr (MODE == kModeDense) {
-              if (ql < nq && key_ok) {
-                bool vis = kid != INT_MAX;
-                if (p.causal && p.positions != nullptr) vis = vis && kid <= ctrl->pos[ql];
-                p.dense[static_cast<size_t>(t0 + ql) * p.ld + key] = vis ? I : -INFINITY;
-              }
-            } else {
-              const bool vis = (ql < nq) && key_ok && (!p.causal || key <= ctrl->pos[ql]);
-              const int b = bin_of(I, ctrl->s_min[ql], ctrl->delta[ql], p.nb);
-              const int th = *reinterpret_cast<volatile int*>(&ctrl->theta[ql]);
-              const bool pass = vis && b >= th;
-              const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
-              if (m != 0) {
-                const int leader = __ffs(m) - 1;
-                int base = 0;
-                if (lane == leader) base = atomicAdd(&ctrl->cnt[ql], __popc(m));
-                base = __shfl_sync(0xFFFFFFFFu, base, leader);
-                if (pass) {
-                  const int slot = base + __popc(m & ((1u << lane) - 1u));
-                  if (slot < p.cap)
-                    p.cand[static_cast<size_t>(t0 + ql) * p.cap + slot] =
-                        cand_pack(I, static_cast<int>(key));
-                  atomicAdd(&hist[ql * p.nb + b], 1);
-                }
+          const float2 pa = head_partials(va, wr[j]);
+          const float2 pb = head_partials(vb, wr[j]);
+          float I = quad_reduce(pa.x, pa.y, pb.x, pb.y, c);
+          const int ql = j * 4 + qh;            // query within the CTA
+          if constexpr (FP8) I = __fmul_rn(I, kscale);
+          if constexpr (MODE == kModeDense) {
+            if (ql < nq && key_ok) {
+              bool vis = kid != INT_MAX;
+              if (p.causal && p.positions != nullptr) vis = vis && kid <= ctrl->pos[ql];
+              p.dense[static_cast<size_t>(t0 + ql) * p.ld + key] = vis ? I : -INFINITY;
+            }
+          } else {
+            const bool vis = (ql < nq) && key_ok && (!p.causal || key <= ctrl->pos[ql]);
+            const int b = bin_of(I, ctrl->s_min[ql], ctrl->delta[ql], p.nb);
+            const int th = *reinterpret_cast<volatile int*>(&ctrl->theta[ql]);
+            const bool pass = vis && b >= th;
+            const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
+            if (m != 0) {
+              const int leader = __ffs(m) - 1;
+              int base = 0;
+              if (lane == leader) base = atomicAdd(&ctrl->cnt[ql], __popc(m));
+              base = __shfl_sync(0xFFFFFFFFu, base, leader);
+              if (pass) {
+                const int slot = base + __popc(m & ((1u << lane) - 1u));
+                if (slot < p.cap)
+                  p.cand[static_cast<size_t>(t0 + ql) * p.cap + slot] =
+                      cand_pack(I, static_cast<int>(key));
+                atomicAdd(&hist[ql * p.nb + b], 1);
               }
             }
           }
