@@ -233,6 +233,28 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
                               const int* positions, int T, long long S, int k,
                               int* out_idx, float* out_score, void* stream);
 
+/*
+ * Decoupled top-k that allocates nothing (no counterpart in the paper: it is
+ * an integration convenience).  For callers that cannot call cudaMalloc -- a
+ * plugin inside an engine that owns all device memory through its own pool,
+ * or a latency-critical path where cudaMalloc's implicit device
+ * synchronisation is not acceptable.  Same computation and output contract as
+ * ltk_decoupled_topk for H = 64, d = 128, ReLU scores, without a handle:
+ * dtype is LTK_BF16 or LTK_FP8_E4M3, causal selects the s <= positions[t]
+ * mask.  Its scratch, the T x S fp32 score matrix, lives in a static device
+ * array of 4,194,304 floats (16 MiB) that every GPU loading the library
+ * holds until process exit; T * S above that returns LTK_ERR_ARG.  The
+ * caller still owns all inputs and outputs.  The first call on each device
+ * looks up that array's device address (with the device current), so make
+ * the first call on a device before any stream capture.  All calls share the
+ * array, so calls that overlap on the GPU race and corrupt each other's
+ * results: serialise them (one stream, or synchronise between calls).
+ */
+ltk_status ltk_decoupled_topk_noalloc(int dtype, int causal, const void* q, const float* q_scale,
+                                      const float* w, const void* k_cache, const float* k_scale,
+                                      const int* positions, int T, long long S, int k,
+                                      int* out_idx, float* out_score, void* stream);
+
 /* Statistics of the last compute call (synchronises its stream). */
 ltk_status ltk_get_stats(ltk_handle* h, ltk_stats* out);
 

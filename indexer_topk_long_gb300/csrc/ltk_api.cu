@@ -677,3 +677,91 @@ ltk_status ltk_get_stats(ltk_handle* h, ltk_stats* out) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decoupled top-k without any allocation
+// ---------------------------------------------------------------------------
+// Some callers cannot call cudaMalloc: a plugin running inside an engine that
+// owns all device memory through its own pool and rejects allocations made
+// behind its back, or a latency-critical path where cudaMalloc's implicit
+// device synchronisation would stall the caller's other streams.  This entry
+// point serves them: it needs no handle, and its only scratch -- the fp32
+// score matrix of the decoupled baseline -- lives in the file-scope device
+// array below.  Every GPU that loads this library holds that array until the
+// process exits.
+namespace {
+
+constexpr long long kNoAllocMaxScores = 4ll << 20;   // T * S <= 4,194,304 (16 MiB of fp32)
+static __device__ __align__(256) float g_noalloc_scores[kNoAllocMaxScores];
+
+constexpr int kNoAllocMaxDevices = 256;
+float* g_noalloc_ptr[kNoAllocMaxDevices] = {};      // device address of the array, per device
+
+// Host code must not use g_noalloc_scores directly: on the host it is only a
+// stand-in for the device symbol.  The device address is looked up once per
+// device, with that device current.
+ltk_status noalloc_scores_for_current_device(float** out) {
+  static std::atomic<int> lock{0};
+  int dev = -1;
+  LTK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return LTK_ERR_UNSUPPORTED;
+  while (lock.exchange(1, std::memory_order_acquire)) {
+  }
+  ltk_status st = LTK_OK;
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scores);
+    if (e == cudaSuccess && p != nullptr)
+      g_noalloc_ptr[dev] = static_cast<float*>(p);
+    else
+      st = cuda_fail(e == cudaSuccess ? cudaErrorInvalidSymbol : e, "cudaGetSymbolAddress");
+  }
+  *out = g_noalloc_ptr[dev];
+  lock.store(0, std::memory_order_release);
+  return st;
+}
+
+}  // namespace
+
+extern "C" ltk_status ltk_decoupled_topk_noalloc(int dtype, int causal, const void* q,
+                                                 const float* q_scale, const float* w,
+                                                 const void* k_cache, const float* k_scale,
+                                                 const int* positions, int T, long long S, int k,
+                                                 int* out_idx, float* out_score, void* stream) {
+  if (dtype != LTK_BF16 && dtype != LTK_FP8_E4M3) return LTK_ERR_ARG;
+  if (T < 0 || S < 1 || S > 0x7FFFFFFFll || k < 1 || k > kMaxK) return LTK_ERR_ARG;
+  if (static_cast<long long>(T) * S > kNoAllocMaxScores) return LTK_ERR_ARG;
+  if (T == 0) return LTK_OK;
+  if (!q || !w || !k_cache || !out_idx || !out_score) return LTK_ERR_ARG;
+  if (!aligned16(q) || !aligned16(w) || !aligned16(k_cache) || !aligned16(out_idx) ||
+      !aligned16(out_score))
+    return LTK_ERR_ARG;
+  if (causal && (positions == nullptr || !aligned16(positions))) return LTK_ERR_ARG;
+  const bool fp8 = dtype == LTK_FP8_E4M3;
+  if (fp8 && (!q_scale || !k_scale || !aligned16(q_scale) || !aligned16(k_scale))) return LTK_ERR_ARG;
+  float* scores = nullptr;
+  const ltk_status st0 = noalloc_scores_for_current_device(&scores);
+  if (st0 != LTK_OK) return st0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUtensorMap q_map, k_map;
+  if (!make_tmap(&q_map, q, fp8, kTcDim, static_cast<unsigned long long>(T) * kTcHeads, 256) ||
+      !make_tmap(&k_map, k_cache, fp8, kTcDim, static_cast<unsigned long long>(S), kTile))
+    return LTK_ERR_CUDA;
+  ScoreParams sp{};
+  sp.w = w;
+  sp.q_scale = q_scale;
+  sp.k_scale = k_scale;
+  sp.positions = causal ? positions : nullptr;
+  sp.key_ids = nullptr;
+  sp.T = T;
+  sp.rows = S;
+  sp.causal = causal ? 1 : 0;
+  sp.dense = scores;
+  sp.ld = S;
+  sp.status = nullptr;
+  LTK_CUDA(launch_score_tc(kModeDense, fp8, q_map, k_map, sp, st));
+  RowTopkParams rp{scores, S, causal ? positions : nullptr, T, S, causal ? 1 : 0, k, out_idx,
+                   out_score, nullptr};
+  LTK_CUDA(launch_row_topk(rp, st));
+  return LTK_OK;
+}

@@ -66,6 +66,7 @@ _SIGS = {
     "ltk_indexer_topk_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _LL, _P, _I, _I, _P, _P, _P]),
     "ltk_decoupled_topk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _LL, _I, _P, _P, _P]),
     "ltk_get_stats": (_I, [_P, ctypes.POINTER(Stats)]),
+    "ltk_decoupled_topk_noalloc": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _I, _LL, _I, _P, _P, _P]),
 }
 
 _LIB = None
