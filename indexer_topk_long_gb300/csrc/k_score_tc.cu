@@ -89,18 +89,27 @@ constexpr size_t smem_bytes(int nb) {
 //
 // Partial weighted head sums of one query for 2 keys: va holds a 16x256b x8
 // load (64 columns of 16 lanes), so thread t (c = t % 4) has heads
-// {8r + 2c + i} of keys t/4 and t/4 + 8; w holds the weights of those heads.
-// Returns the two partial sums sum_h w[h] * max(0, x[h]) (packed fp32x2 FMA).
-__device__ __forceinline__ float2 head_partials(const float* va, const float (&w)[16]) {
-  float2 a0 = make_float2(0.f, 0.f), a1 = a0;
+// h = 8r + 2c + {0, 1} of keys t/4 and t/4 + 8; w2[r] packs the weights of
+// that head pair.  Each packed FMA covers one head pair of one key.  The even
+// head's ReLU is max(x, 0) (ALU pipe); the odd head uses x + |x| = 2 max(x, 0)
+// (FMA pipe) and its accumulator half is halved at the end, which is exact, so
+// the sums equal sum_h w[h] * max(0, x[h]) accumulated in this order.
+__device__ __forceinline__ float relu_twice(float x) { return __fadd_rn(x, fabsf(x)); }
+
+__device__ __forceinline__ float fold_pair(unsigned long long acc) {
+  const float lo = __uint_as_float(static_cast<uint32_t>(acc));
+  const float hi = __uint_as_float(static_cast<uint32_t>(acc >> 32));
+  return __fmaf_rn(hi, 0.5f, lo);
+}
+
+__device__ __forceinline__ float2 head_partials(const float* va, const unsigned long long (&w2)[8]) {
+  unsigned long long a0 = 0ull, a1 = 0ull;   // (+0.f, +0.f)
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    ffma2(a0, make_float2(fmaxf(va[4 * r + 0], 0.f), fmaxf(va[4 * r + 2], 0.f)),
-          make_float2(w[2 * r], w[2 * r]));
-    ffma2(a1, make_float2(fmaxf(va[4 * r + 1], 0.f), fmaxf(va[4 * r + 3], 0.f)),
-          make_float2(w[2 * r + 1], w[2 * r + 1]));
+    ffma2_acc(a0, fmaxf(va[4 * r + 0], 0.f), relu_twice(va[4 * r + 1]), w2[r]);
+    ffma2_acc(a1, fmaxf(va[4 * r + 2], 0.f), relu_twice(va[4 * r + 3]), w2[r]);
   }
-  return make_float2(__fadd_rn(a0.x, a1.x), __fadd_rn(a0.y, a1.y));
+  return make_float2(fold_pair(a0), fold_pair(a1));
 }
 
 // Reduce-scatter over the quad of threads that hold the same 4 keys
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 refresh_threshold(hist + ql * p.nb, p.nb, p.k,
                                   reinterpret_cast<volatile int*>(&ctrl->theta[ql]), lane);
             } else {
-              __nanosleep(200);
+              __nanosleep(1000);
               bool expired = globaltimer_ns() - t_prog > kWaitLimitNs;
               expired = __shfl_sync(0xFFFFFFFFu, expired, 0);
               if (expired) {
@@ -343,31 +352,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c = lane & 3;
       const int row = lq * 32 + (lane >> 2) + 8 * c;   // key row this thread finishes
       const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
-      // weights of this thread's 16 heads {8r + 2c + i} for query qh of each half
-      float wr[2][16];
+      // weight pairs of this thread's heads {8r + 2c, 8r + 2c + 1}, query qh of each half
+      unsigned long long wr[2][8];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const float4* src = reinterpret_cast<const float4*>(w_s + (j * 4 + qh) * kTcHeads + c * 16);
+        const ulonglong2* src =
+            reinterpret_cast<const ulonglong2*>(w_s + (j * 4 + qh) * kTcHeads + c * 16);
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          const float4 x = src[v4];
-          wr[j][4 * v4 + 0] = x.x;
-          wr[j][4 * v4 + 1] = x.y;
-          wr[j][4 * v4 + 2] = x.z;
-          wr[j][4 * v4 + 3] = x.w;
+        for (int v2 = 0; v2 < 4; ++v2) {
+          const ulonglong2 x = src[v2];
+          wr[j][2 * v2] = x.x;
+          wr[j][2 * v2 + 1] = x.y;
         }
       }
+      // per-warp constants for the two queries (one per half)
+      const int rows_i = static_cast<int>(p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF);
+      int last_key[2];
+      float qs_min[2], qdelta[2];
+      int* qhist[2];
+      unsigned long long* qcand[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int ql = j * 4 + qh;
+        const bool valid = ql < nq;
+        // a key is visible iff key <= last_key (causal position and cache end)
+        last_key[j] = valid ? min(p.causal ? ctrl->pos[ql] : 0x7FFFFFFF, rows_i - 1) : -1;
+        if constexpr (MODE == kModeFilter) {
+          qs_min[j] = ctrl->s_min[ql];
+          qdelta[j] = ctrl->delta[ql];
+          qhist[j] = hist + ql * p.nb;
+          qcand[j] = p.cand + static_cast<size_t>(valid ? t0 + ql : 0) * p.cap;
+        }
+      }
+      const uint32_t acc_full0 = smem_u32(&ctrl->acc_full[0]);
+      const uint32_t acc_empty0 = smem_u32(&ctrl->acc_empty[0]);
+      const uint32_t tq0 = tmem + lane_base + qh * kTcHeads;
       for (int i = 0; i < n_tiles; ++i) {
-        const long long key = static_cast<long long>(i) * kTile + row;
-        const bool key_ok = key < p.rows;
+        const int key = i * kTile + row;
+        const bool key_ok = key < rows_i;
         float kscale = 1.f;
         if constexpr (FP8) kscale = key_ok ? p.k_scale[key] : 0.f;
-        int kid = static_cast<int>(key);
+        int kid = key;
         if (MODE == kModeDense && p.key_ids != nullptr) kid = key_ok ? p.key_ids[key] : INT_MAX;
         bool stop = false;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          bool ok = mbar_wait(smem_u32(&ctrl->acc_full[j]), i & 1, abort_flag, p.status);
+          bool ok = mbar_wait(acc_full0 + 8 * j, i & 1, abort_flag, p.status);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) {
             stop = true;
@@ -375,14 +405,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           // read the query's 64 columns, then hand the TMEM half back at once
-          const uint32_t ta = tmem + lane_base + j * kN + qh * kTcHeads;
+          const uint32_t ta = tq0 + j * kN;
           float va[32], vb[32];
           tmem_ld16x256b_x8(ta, va);
           tmem_ld16x256b_x8(ta + (16u << 16), vb);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctrl->acc_empty[j]));
+          if (lane == 0) mbar_arrive(acc_empty0 + 8 * j);
           const float2 pa = head_partials(va, wr[j]);
           const float2 pb = head_partials(vb, wr[j]);
           float I = quad_reduce(pa.x, pa.y, pb.x, pb.y, c);
@@ -395,10 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               p.dense[static_cast<size_t>(t0 + ql) * p.ld + key] = vis ? I : -INFINITY;
             }
           } else {
-            const bool vis = (ql < nq) && key_ok && (!p.causal || key <= ctrl->pos[ql]);
-            const int b = bin_of(I, ctrl->s_min[ql], ctrl->delta[ql], p.nb);
+            const int b = bin_of(I, qs_min[j], qdelta[j], p.nb);
             const int th = *reinterpret_cast<volatile int*>(&ctrl->theta[ql]);
-            const bool pass = vis && b >= th;
+            const bool pass = key <= last_key[j] && b >= th;
             const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
             if (m != 0) {
               const int leader = __ffs(m) - 1;
@@ -407,10 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               base = __shfl_sync(0xFFFFFFFFu, base, leader);
               if (pass) {
                 const int slot = base + __popc(m & ((1u << lane) - 1u));
-                if (slot < p.cap)
-                  p.cand[static_cast<size_t>(t0 + ql) * p.cap + slot] =
-                      cand_pack(I, static_cast<int>(key));
-                atomicAdd(&hist[ql * p.nb + b], 1);
+                if (slot < p.cap) qcand[j][slot] = cand_pack(I, key);
+                atomicAdd(&qhist[j][b], 1);
               }
             }
           }

@@ -55,9 +55,8 @@ __device__ __forceinline__ void raise_status(int* status, int code) {
 // used by the Sample, Filter and Select stages alike.
 __device__ __forceinline__ int bin_of(float I, float s_min, float delta, int nb) {
   const float f = __fmul_rn(__fsub_rn(I, s_min), delta);
-  if (!(f >= 0.f)) return 0;
-  if (f >= static_cast<float>(nb)) return nb - 1;
-  return static_cast<int>(f);
+  // fmaxf returns 0 for a NaN f; truncation of the clamped value is the floor
+  return __float2int_rz(fminf(fmaxf(f, 0.f), static_cast<float>(nb - 1)));
 }
 
 // Order-preserving map fp32 -> uint32 (larger float -> larger integer).
@@ -124,6 +123,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or the hint (ns) expires.  Used only after a short spin, for
+// waits that are already long.
+constexpr uint32_t kSuspendHintNs = 200000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the completion of phase `parity`.  Returns false when the
 // CTA's abort flag is set by another role or when the wait exceeds
 // kWaitLimitNs (then it sets the abort flag and the device status itself).
@@ -133,7 +148,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       if (abort_flag != nullptr) *abort_flag = 1;
@@ -249,6 +264,15 @@ __device__ __forceinline__ void tmem_ld16x256b_x8(uint32_t taddr, float* v, floa
       : "r"(taddr), "f"(after));
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Packed fp32x2 fused multiply-add on a bit-packed accumulator pair:
+// acc = (a0, a1) * wpair + acc, lane-wise (sm_100+).
+__device__ __forceinline__ void ffma2_acc(unsigned long long& acc, float a0, float a1,
+                                          unsigned long long wpair) {
+  unsigned long long A;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(A), "l"(wpair));
 }
 
 // Packed fp32x2 fused multiply-add (sm_100+): acc = a * b + acc, lane-wise.
