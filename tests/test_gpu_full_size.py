@@ -1,0 +1,108 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+Each chunk runs with the previous chunk's top-3k as the sample (the previous
+chunk is run first, as the prefill would).  The CPU oracle checks a seeded
+subset of queries element by element (always the first and last query of the
+chunk); every query is checked for the invariants that hold at any size
+(sorted output, distinct indices, no index beyond the query's position,
+exactly min(k, V) valid entries), and at 128K and 1M the same-GPU decoupled
+baseline -- a second, independent selection path over the same fp32 scores --
+must return identical results for all queries.
+"""
+import numpy as np
+import pytest
+
+import oracle.indexer_topk as orc
+from indexer_topk_long_gb300 import IndexerTopK, datagen
+from parity import check_tolerant, to_device
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _invariants(idx, sc, positions, S, k):
+    V = np.minimum(positions.astype(np.int64) + 1, S)
+    n = np.minimum(V, k)
+    T = idx.shape[0]
+    cols = np.arange(k)[None, :]
+    valid = cols < n[:, None]
+    assert np.all((idx >= 0) == valid), "valid-entry count"
+    assert np.all(np.isneginf(sc[~valid])), "padding scores"
+    assert np.all(idx[valid] <= np.repeat(positions, n)), "index beyond the query's position"
+    s_sorted = np.sort(idx, axis=1)
+    dup = (s_sorted[:, 1:] == s_sorted[:, :-1]) & (s_sorted[:, 1:] >= 0)
+    assert not dup.any(), "duplicate index"
+    a, b = sc[:, :-1], sc[:, 1:]
+    ia, ib = idx[:, :-1], idx[:, 1:]
+    both = valid[:, 1:]
+    ok = (a > b) | ((a == b) & (ia < ib))
+    assert np.all(ok[both]), "output order"
+    del T
+
+
+def _sample_queries(T, n, seed):
+    rng = np.random.default_rng(seed)
+    q = set(rng.choice(T, size=n - 2, replace=False).tolist()) | {0, T - 1}
+    return sorted(q)
+
+
+def _chunk_pair(prev_name, cur_name, dtype, n_check, decoupled):
+    import torch
+    wl = datagen.WORKLOADS[cur_name]
+    keys = datagen.keys_fp32(wl.S, wl.d)
+    prev = datagen.workload_inputs(prev_name, dtype=dtype, keys=keys)
+    cur = datagen.workload_inputs(cur_name, dtype=dtype, keys=keys)
+    op = IndexerTopK(max_T=wl.T, max_S=wl.S, k=wl.k, dtype=dtype,
+                     enable_decoupled=1 if decoupled else 0)
+    dp, dc = to_device(prev), to_device(cur)
+    S_prev = prev.S
+    ks = None if dc["k_scale"] is None else dc["k_scale"][:S_prev]
+    p_idx, p_sc = op(dp["q"], dp["w"], dc["k_cache"][:S_prev], dp["positions"], k=wl.k,
+                     q_scale=dp["q_scale"], k_scale=ks)
+    sample = op.make_sample(p_idx, wl.S, 3 * wl.k)
+    idx, sc = op(dc["q"], dc["w"], dc["k_cache"], dc["positions"], k=wl.k, prev_topk=sample,
+                 q_scale=dc["q_scale"], k_scale=dc["k_scale"])
+    torch.cuda.synchronize()
+    st = op.stats()
+    assert st["device_status"] == 0 and st["visible_pairs"] == wl.visible_pairs
+    out = {"idx": idx.cpu().numpy(), "sc": sc.cpu().numpy(), "stats": st,
+           "prev_idx": p_idx.cpu().numpy(), "prev_sc": p_sc.cpu().numpy()}
+    if decoupled:
+        d_idx, d_sc = op.decoupled(dc["q"], dc["w"], dc["k_cache"], dc["positions"], k=wl.k,
+                                   q_scale=dc["q_scale"], k_scale=dc["k_scale"])
+        torch.cuda.synchronize()
+        out["dec_identical"] = bool(torch.equal(d_idx, idx) and torch.equal(d_sc, sc))
+    op.close()
+    del dp, dc
+    torch.cuda.empty_cache()
+    keys64 = orc.widen_keys(cur)
+    q = _sample_queries(wl.T, n_check, 7)
+    check_tolerant(cur, out["idx"], out["sc"], wl.k, queries=q, keys64=keys64)
+    _invariants(out["idx"], out["sc"], cur.positions, wl.S, wl.k)
+    # the previous chunk, too (its sample was random)
+    qp = _sample_queries(prev.T, 4, 8)
+    check_tolerant(prev, out["prev_idx"], out["prev_sc"], wl.k, queries=qp,
+                   keys64=keys64[:prev.S])
+    _invariants(out["prev_idx"], out["prev_sc"], prev.positions, prev.S, wl.k)
+    return out
+
+
+def test_128k_two_consecutive_chunks():
+    out = _chunk_pair("128k_chunk1", "128k_chunk2", "bf16", 24, decoupled=True)
+    assert out["dec_identical"]
+    assert out["stats"]["n_overflow"] == 0
+
+
+def test_256k_chunk():
+    out = _chunk_pair("256k_prev", "256k", "bf16", 12, decoupled=False)
+    assert out["stats"]["n_overflow"] == 0
+
+
+def test_1m_chunk_bf16():
+    out = _chunk_pair("1m_prev", "1m", "bf16", 10, decoupled=True)
+    assert out["dec_identical"]
+    assert out["stats"]["n_overflow"] == 0
+
+
+def test_1m_chunk_fp8():
+    out = _chunk_pair("1m_prev", "1m", "fp8", 8, decoupled=False)
+    assert out["stats"]["n_overflow"] == 0
