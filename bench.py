@@ -71,6 +71,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(pairs_per_step: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Visible pairs scored by all ranks (one chunk each per step) per second."""
+    return world * pairs_per_step * steps / (elapsed_ms * 1e-3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -319,14 +335,11 @@ def main():
     st = op.stats()
     op.set_timing(False)
     launches = st["launches"] - launches0
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     pairs_step = st["visible_pairs"]
     assert pairs_step == wl.visible_pairs, (pairs_step, wl.visible_pairs)
     ms_per_step = elapsed_ms / args.steps
-    value = world * pairs_step * args.steps / (elapsed_ms * 1e-3)
+    value = whole_job_value(pairs_step, args.steps, world, elapsed_ms)
 
     peaks, peaks_kind = measured_peaks()
     bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
@@ -386,15 +399,11 @@ def main():
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None) + \
             sample.numel() * 4
         d2h = sum(v.numel() * v.element_size() for v in hout)
-        line["e2e"] = {"value": world * pairs_step * args.steps / (e_ms * 1e-3), "unit": UNIT,
+        line["e2e"] = {"value": whole_job_value(pairs_step, args.steps, world, e_ms), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": e_ms / args.steps,
                        "call": "ltk_indexer_topk_host (pinned host buffers, copies inside)"}
