@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ltk", "reference"], default="ltk")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="1m")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["retrieval"], default="1m")
     ap.add_argument("--dtype", choices=["bf16", "fp8"], default="bf16")
     ap.add_argument("--queries", type=int, default=0,
                     help="run only the first N queries of the chunk (profiling a single wave)")
@@ -264,10 +264,131 @@ def run_reference(args):
     return 0
 
 
+RETRIEVAL = dict(T=1024, N=8388608, d=768, k=1000, sample=3000)
+RETRIEVAL_METRIC = "scored query-vector pairs/s, vector retrieval 1024 x 8.4M, d=768, k=1000 (1 GB300)"
+
+
+def run_retrieval(args):
+    """Vector-retrieval workload: one head, plain inner product, no mask."""
+    import numpy as np
+    import torch
+    from indexer_topk_long_gb300 import IndexerTopK, datagen
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    R = RETRIEVAL
+    T = args.queries or R["T"]
+    q, c = datagen.retrieval_inputs_torch(R["N"], T, R["d"], seed=20260715 + rank, device=dev)
+    w = torch.ones((T, 1), dtype=torch.float32, device=dev)
+    qi, ci = q.view(torch.int16), c.view(torch.int16)
+    op = IndexerTopK(max_T=T, max_S=R["N"], k=R["k"], heads=1, dim=R["d"], sample_size=R["sample"],
+                     enable_host_io=0 if args.no_e2e else 1)
+    stream = torch.cuda.current_stream()
+    out = (torch.empty((T, R["k"]), dtype=torch.int32, device=dev),
+           torch.empty((T, R["k"]), dtype=torch.float32, device=dev))
+    step = lambda: op(qi, w, ci, None, k=R["k"], out=out)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    launches0 = op.stats()["launches"]
+    op.set_timing(True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(None)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    st = op.stats()
+    op.set_timing(False)
+    elapsed = max_over_ranks(e0.elapsed_time(e1), dev)
+    pairs = T * R["N"]
+    assert st["visible_pairs"] == pairs and st["device_status"] == 0
+    peaks, kind = measured_peaks()
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    flop = 2 * R["d"] * pairs
+    achieved = flop / (st["ms_filter"] * 1e-3) / 1e12
+    line = {
+        "metric": RETRIEVAL_METRIC, "value": whole_job_value(pairs, args.steps, world, elapsed),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (clustered Gaussian corpus; MSMARCO unavailable)",
+        "config": {"workload": f"vector retrieval: {T} queries x {R['N']} corpus rows, d={R['d']}, "
+                               f"k={R['k']}, H=1, no ReLU, no mask, {R['sample']} random sample rows",
+                   "l2": "inputs larger than L2 (corpus 12.9 GB)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "retrieval_tc_kernel<filter>",
+                     "peak_source": f"{kind} bf16 sustained", "algorithmic_flop_per_launch": flop},
+        "gpu_launches": st["launches"] - launches0, "clocks": clock_info,
+        "stages_ms": {"sample": st["ms_sample"], "filter": st["ms_filter"], "select": st["ms_select"],
+                      "rescue": st["ms_rescue"]},
+        "candidates_per_query": st["cand_written"] / T, "n_overflow": st["n_overflow"],
+    }
+    if not args.no_decoupled and world == 1:
+        dec = IndexerTopK(max_T=T, max_S=R["N"], k=R["k"], heads=1, dim=R["d"], enable_decoupled=1)
+        di, ds = dec.decoupled(qi, w, ci, None, k=R["k"])
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        dec.decoupled(qi, w, ci, None, k=R["k"], out=(di, ds))
+        a1.record(stream)
+        torch.cuda.synchronize()
+        line["decoupled"] = {"ms_per_step": a0.elapsed_time(a1),
+                             "identical_output": bool(torch.equal(di, out[0]) and torch.equal(ds, out[1]))}
+        dec.close()
+        del dec, di, ds
+        torch.cuda.empty_cache()
+    if not args.no_e2e:
+        hq, hw, hc = qi.cpu().pin_memory(), w.cpu().pin_memory(), ci.cpu().pin_memory()
+        hout = (torch.empty((T, R["k"]), dtype=torch.int32, pin_memory=True),
+                torch.empty((T, R["k"]), dtype=torch.float32, pin_memory=True))
+        op.topk_host(hq, hw, hc, None, k=R["k"], out=hout)
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            op.topk_host(hq, hw, hc, None, k=R["k"], out=hout)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(a0.elapsed_time(a1), dev)
+        line["e2e"] = {"value": whole_job_value(pairs, args.steps, world, e_ms), "unit": UNIT,
+                       "h2d_bytes_per_step": hq.numel() * 2 + hw.numel() * 4 + hc.numel() * 2,
+                       "d2h_bytes_per_step": T * R["k"] * 8, "ms_per_step": e_ms / args.steps}
+    if not args.no_cpu and world == 1 and rank == 0:
+        import oracle.indexer_topk as orc
+        n_rows = 1 << 20
+        sel = [0, T // 2, T - 1]
+        qh = qi[sel].cpu().numpy().view(np.uint16)
+        ch = ci[:n_rows].cpu().numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        orc.retrieval_topk(qh, ch, R["k"])
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": len(sel) * n_rows / secs, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle", "seconds": secs,
+                                "sample": f"{len(sel)} queries against the first {n_rows} corpus rows"}
+    op.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "retrieval":
+        return run_retrieval(args)
     import numpy as np
     import torch
     from indexer_topk_long_gb300 import IndexerTopK

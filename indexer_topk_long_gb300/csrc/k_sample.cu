@@ -156,11 +156,16 @@ __device__ uint32_t block_select_u32(const uint32_t* vals, int m, int r, unsigne
   return prefix;
 }
 
-// Per query: range of the visible sample scores, delta = nb / (s_max - s_min),
-// and the initial threshold bin = bin of the k-th largest visible sample score
-// minus one (one bin of slack so that a score computed in a different rounding
-// order could never lift the start above the true k-th score's bin).  With
-// fewer than k visible sample keys the threshold starts at 0.
+// Per query, from the visible sample scores: the equal-width bins and the
+// start threshold bin.  Bins below the start threshold are never used (the
+// threshold only rises), so the bins span from just below the sample's k-th
+// largest score s_k up to s_max + (s_max - s_k): the span above s_k, doubled
+// as headroom for top-k scores beyond the sample's maximum (a small sample of a
+// large cache rarely contains the true top scores).  s_k sits three bins above
+// the lower end; the start threshold is bin(s_k) - 1, one bin of slack below
+// it, and everything under the range clamps into bin 0 and is rejected.  With
+// fewer than k visible sample keys (or no spread above s_k) the bins cover
+// [s_min, s_max + (s_max - s_min)] and the threshold starts at 0.
 __global__ void __launch_bounds__(kStatsThreads) sample_stats_kernel(const SampleStatsParams p) {
   extern __shared__ uint32_t s_ord[];
   __shared__ unsigned hist256[256];
@@ -208,17 +213,27 @@ __global__ void __launch_bounds__(kStatsThreads) sample_stats_kernel(const Sampl
   mx = red_max[0];
   cnt = red_cnt[0];
   float smin = 0.f, delta = 0.f;
-  if (cnt > 0) {
-    smin = mn;
-    if (mx > mn) {
-      delta = __fdiv_rn(static_cast<float>(p.nb), __fsub_rn(mx, mn));
+  int theta = 0;
+  bool ranged = false;
+  if (cnt >= p.k && p.k > 0) {
+    const float sk = unord_f32(block_select_u32(s_ord, p.n, p.k, hist256, sh_state));
+    const float span = __fsub_rn(mx, sk);
+    if (span > 0.f) {
+      const float hi = __fadd_rn(mx, span);
+      delta = __fdiv_rn(static_cast<float>(p.nb - 3), __fsub_rn(hi, sk));
       if (!(delta <= 1e30f)) delta = 1e30f;
+      smin = __fsub_rn(sk, __fdiv_rn(3.f, delta));
+      theta = max(0, bin_of(sk, smin, delta, p.nb) - 1);
+      ranged = true;
     }
   }
-  int theta = 0;
-  if (cnt >= p.k && p.k > 0) {
-    const uint32_t kth = block_select_u32(s_ord, p.n, p.k, hist256, sh_state);
-    theta = max(0, bin_of(unord_f32(kth), smin, delta, p.nb) - 1);
+  if (!ranged && cnt > 0) {
+    smin = mn;
+    theta = 0;
+    if (mx > mn) {
+      delta = __fdiv_rn(static_cast<float>(p.nb), __fmul_rn(2.f, __fsub_rn(mx, mn)));
+      if (!(delta <= 1e30f)) delta = 1e30f;
+    }
   }
   if (threadIdx.x == 0) {
     p.s_min[t] = smin;

@@ -446,8 +446,38 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 
 constexpr int kRescueThreads = 256;
 
+// One head (vector retrieval): I[s] = w[t] * f(q[t] . c[s]), f = ReLU or identity.
+__device__ void rescue_row_scores_one_head(const RescueParams& p, int t, int V, float* row,
+                                           float* qf) {
+  const int d = p.dim;
+  const uint16_t* q = static_cast<const uint16_t*>(p.q) + static_cast<size_t>(t) * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) qf[i] = __uint_as_float(static_cast<uint32_t>(q[i]) << 16);
+  const float wt = p.w[t];
+  __syncthreads();
+  for (int s = threadIdx.x; s < V; s += blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k_cache) +
+                                                      static_cast<size_t>(s) * d);
+    float acc = 0.f;
+    for (int v8 = 0; v8 < d / 8; ++v8) {
+      const uint4 r = src[v8];
+      const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc = __fmaf_rn(qf[8 * v8 + 2 * j], __uint_as_float(w4[j] << 16), acc);
+        acc = __fmaf_rn(qf[8 * v8 + 2 * j + 1], __uint_as_float(w4[j] & 0xFFFF0000u), acc);
+      }
+    }
+    row[s] = __fmul_rn(p.relu ? fmaxf(acc, 0.f) : acc, wt);
+  }
+  __syncthreads();
+}
+
 __device__ void rescue_row_scores(const RescueParams& p, int t, int V, float* row, float* qf,
                                   float* wf) {
+  if (p.heads == 1) {
+    rescue_row_scores_one_head(p, t, V, row, qf);
+    return;
+  }
   const int H = kTcHeads, d = kTcDim;
   const size_t qoff = static_cast<size_t>(t) * H * d;
   for (int i = threadIdx.x; i < H * d; i += blockDim.x) {

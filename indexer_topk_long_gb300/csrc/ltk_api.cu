@@ -24,6 +24,7 @@ struct ltk_handle {
   int cap = 0;
   int n_pad_max = 0;
   int rescue_rows = 0;
+  int num_sms = 148;
   size_t elem = 2;
   // workspace
   float* samp_scores = nullptr;        // [max_T, n_pad_max]
@@ -37,6 +38,7 @@ struct ltk_handle {
   unsigned long long* cand = nullptr;  // [max_T, cap]
   int* cnt = nullptr;                  // [max_T]
   int* ovf = nullptr;                  // [2 + max_T]: count, next, list
+  int* ghist = nullptr;                // [max_T, n_bins] per-query histograms shared by CTAs (retrieval)
   float* rescue_scratch = nullptr;     // [rescue_rows, max_S]
   float* dense = nullptr;              // [max_T, max_S] (decoupled baseline)
   int* status = nullptr;               // [1]
@@ -95,9 +97,10 @@ long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
 int derived_cap(int k, long long max_S) {
   // Expected candidates of a streaming threshold grow like k * (1 + ln(S / k));
-  // the default keeps a 1.5x margin over k * (4 + ln(S / k)), never above S.
+  // the default keeps a 1.5x margin over k * (4 + ln(S / k)) plus 2048 records
+  // (small k starts from a loose sample threshold), never above S.
   const double ratio = static_cast<double>(max_S) / static_cast<double>(k);
-  const double est = k * (4.0 + std::log(ratio > 1.0 ? ratio : 1.0)) * 1.5;
+  const double est = k * (4.0 + std::log(ratio > 1.0 ? ratio : 1.0)) * 1.5 + 2048.0;
   long long cap = round_up(static_cast<long long>(est), 1024);
   const long long s_cap = round_up(max_S, 1024);
   if (cap > s_cap) cap = s_cap;
@@ -105,6 +108,9 @@ int derived_cap(int k, long long max_S) {
   if (cap > (1ll << 30)) cap = 1ll << 30;
   return static_cast<int>(cap);
 }
+
+// One head, plain inner product: the vector-retrieval shape.
+bool is_retrieval(const ltk_config* c) { return c->heads == 1; }
 
 ltk_status validate_config(const ltk_config* c) {
   if (c == nullptr) return LTK_ERR_ARG;
@@ -115,6 +121,12 @@ ltk_status validate_config(const ltk_config* c) {
   if (c->sample_size < 0 || c->sample_size > kMaxSample) return LTK_ERR_ARG;
   if (c->cand_cap < 0 || c->refresh_interval < 0 || c->rescue_rows < 0) return LTK_ERR_ARG;
   if (!is_pow2(c->n_bins) || c->n_bins < 32) return LTK_ERR_ARG;
+  if (is_retrieval(c)) {
+    if (c->dtype != LTK_BF16 || c->causal || c->dim % 64 != 0 || c->dim > kRetrievalMaxDim ||
+        c->n_bins > kRetrievalMaxBins || (c->relu != 0 && c->relu != 1))
+      return LTK_ERR_UNSUPPORTED;
+    return LTK_OK;
+  }
   if (c->heads != kTcHeads || c->dim != kTcDim || c->relu != 1) return LTK_ERR_UNSUPPORTED;
   if (c->n_bins > score_tc_max_bins(c->dtype == LTK_FP8_E4M3)) return LTK_ERR_UNSUPPORTED;
   return LTK_OK;
@@ -141,6 +153,7 @@ Sizes compute_sizes(const ltk_config* c) {
   b += static_cast<unsigned long long>(s.n_pad_max) * 4 * 2;            // scales + ids
   b += kMaxSample * 4ull;                             // random sample ids
   b += T * 4 * 4;                                     // s_min, delta, theta0, cnt
+  if (is_retrieval(c)) b += T * static_cast<unsigned long long>(c->n_bins) * 4;   // shared histograms
   b += T * static_cast<unsigned long long>(s.cap) * 8;  // candidate lists
   b += (T + 2) * 4;                                   // overflow list
   b += static_cast<unsigned long long>(s.rescue_rows) * S * 4;   // rescue rows
@@ -195,7 +208,7 @@ cudaError_t alloc(T** p, unsigned long long bytes) {
 }
 
 void free_all(ltk_handle* h) {
-  void* ptrs[] = {h->samp_scores, h->k_samp,  h->k_scale_samp, h->key_ids_pad,  h->sample_tmp,
+  void* ptrs[] = {h->ghist, h->samp_scores, h->k_samp, h->k_scale_samp, h->key_ids_pad, h->sample_tmp,
                   h->s_min,       h->delta,   h->theta0,       h->cand,         h->cnt,
                   h->ovf,         h->rescue_scratch, h->dense, h->status,       h->ms.counts,
                   h->ms.keys,     h->ms.hist, h->ms.state,     h->io_q,         h->io_qs,
@@ -255,6 +268,21 @@ ltk_status validate_call(const ltk_handle* h, const CallArgs& a) {
   return LTK_OK;
 }
 
+// The scorer for the handle's shape: the indexer kernel (H = 64, d = 128) or
+// the retrieval kernel (one head).
+cudaError_t launch_scorer(const ltk_handle* h, int mode, const CUtensorMap& qm, const CUtensorMap& km,
+                          const ScoreParams& p, cudaStream_t st) {
+  const ltk_config& c = h->cfg;
+  if (is_retrieval(&c))
+    return launch_retrieval_tc(mode, qm, km, p, c.dim, c.relu, h->ghist, h->num_sms, st);
+  return launch_score_tc(mode, c.dtype == LTK_FP8_E4M3, qm, km, p, st);
+}
+
+// Rows of q seen by TMA: [T * H, d].
+unsigned long long q_rows(const ltk_config& c, int T) {
+  return static_cast<unsigned long long>(T) * c.heads;
+}
+
 ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int n_prev,
                      cudaStream_t st) {
   const ltk_config& c = h->cfg;
@@ -288,7 +316,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   LTK_CUDA(launch_gather_keys(a.k_cache, a.k_scale, static_cast<int>(h->elem), c.dim, h->key_ids_pad,
                               n_pad, h->k_samp, h->k_scale_samp, st));
   CUtensorMap q_map, ks_map, k_map;
-  if (!make_tmap(&q_map, a.q, fp8, c.dim, static_cast<unsigned long long>(a.T) * c.heads, 256) ||
+  if (!make_tmap(&q_map, a.q, fp8, c.dim, q_rows(c, a.T), 256) ||
       !make_tmap(&ks_map, h->k_samp, fp8, c.dim, n_pad, kTile) ||
       !make_tmap(&k_map, a.k_cache, fp8, c.dim, static_cast<unsigned long long>(a.S), kTile))
     return LTK_ERR_CUDA;
@@ -304,7 +332,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   sp.dense = h->samp_scores;
   sp.ld = n_pad;
   sp.status = h->status;
-  LTK_CUDA(launch_score_tc(kModeDense, fp8, q_map, ks_map, sp, st));
+  LTK_CUDA(launch_scorer(h, kModeDense, q_map, ks_map, sp, st));
   SampleStatsParams stp{h->samp_scores, n_pad, n_pad, a.T, a.k, c.n_bins, h->s_min, h->delta, h->theta0};
   LTK_CUDA(launch_sample_stats(stp, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
@@ -329,7 +357,11 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   fp.k = a.k;
   fp.refresh_interval = c.refresh_interval;
   fp.status = h->status;
-  LTK_CUDA(launch_score_tc(kModeFilter, fp8, q_map, k_map, fp, st));
+  if (is_retrieval(&c)) {
+    LTK_CUDA(cudaMemsetAsync(h->cnt, 0, static_cast<size_t>(a.T) * sizeof(int), st));
+    LTK_CUDA(cudaMemsetAsync(h->ghist, 0, static_cast<size_t>(a.T) * c.n_bins * sizeof(int), st));
+  }
+  LTK_CUDA(launch_scorer(h, kModeFilter, q_map, k_map, fp, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[2], st));
 
   // ---- Select (Methodology step 3)
@@ -404,6 +436,11 @@ ltk_status ltk_config_init(ltk_config* cfg, int heads, int dim, int k, int max_T
   cfg->enable_decoupled = 0;
   cfg->rescue_rows = 16;
   cfg->enable_host_io = 0;
+  if (heads == 1) {   // vector retrieval: plain inner product over the whole corpus
+    cfg->relu = 0;
+    cfg->causal = 0;
+    cfg->n_bins = kRetrievalMaxBins;
+  }
   return LTK_OK;
 }
 
@@ -429,6 +466,7 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
   h->rescue_rows = z.rescue_rows;
   h->elem = z.elem;
   cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   const unsigned long long T = static_cast<unsigned long long>(cfg->max_T > 0 ? cfg->max_T : 1);
   const unsigned long long S = static_cast<unsigned long long>(cfg->max_S);
   const unsigned long long np = static_cast<unsigned long long>(h->n_pad_max);
@@ -443,6 +481,7 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
   step(alloc(&h->s_min, T * 4));
   step(alloc(&h->delta, T * 4));
   step(alloc(&h->theta0, T * 4));
+  if (is_retrieval(cfg)) step(alloc(&h->ghist, T * static_cast<unsigned long long>(cfg->n_bins) * 4));
   step(alloc(&h->cand, T * static_cast<unsigned long long>(h->cap) * 8));
   step(alloc(&h->cnt, T * 4));
   step(alloc(&h->ovf, (T + 2) * 4));
@@ -588,7 +627,7 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   LTK_CUDA(cudaMemsetAsync(h->pairs, 0, sizeof(unsigned long long), st));
   LTK_CUDA(cudaMemsetAsync(h->ovf, 0, 2 * sizeof(int), st));
   CUtensorMap q_map, k_map;
-  if (!make_tmap(&q_map, q, fp8, c.dim, static_cast<unsigned long long>(T) * c.heads, 256) ||
+  if (!make_tmap(&q_map, q, fp8, c.dim, q_rows(c, T), 256) ||
       !make_tmap(&k_map, k_cache, fp8, c.dim, static_cast<unsigned long long>(S), kTile))
     return LTK_ERR_CUDA;
   ScoreParams sp{};
@@ -604,7 +643,7 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   sp.ld = S;
   sp.status = h->status;
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
-  LTK_CUDA(launch_score_tc(kModeDense, fp8, q_map, k_map, sp, st));
+  LTK_CUDA(launch_scorer(h, kModeDense, q_map, k_map, sp, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[2], st));
   RowTopkParams rp{h->dense, S, c.causal ? positions : nullptr, T, S, c.causal, k, out_idx, out_score,
                    h->pairs};

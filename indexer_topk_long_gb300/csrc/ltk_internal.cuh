@@ -24,6 +24,8 @@ constexpr int kTcHeads = 64;            // H of the tensor-core indexer path
 constexpr int kTcDim = 128;             // d of the tensor-core indexer path
 constexpr int kTcQPB = 8;               // queries per CTA of the scorer
 constexpr int kSelBins = 2048;          // bins of the Select stage's re-binning
+constexpr int kRetrievalMaxBins = 64;   // gate bins of the retrieval scorer (shared-memory bound)
+constexpr int kRetrievalMaxDim = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
 // Device status word values (same numbering as ltk_status).
@@ -356,6 +358,15 @@ cudaError_t launch_score_tc(int mode, bool fp8, const CUtensorMap& q_map, const 
                             const ScoreParams& p, cudaStream_t stream);
 size_t score_tc_smem_bytes(int mode, bool fp8, int nb);
 int score_tc_max_bins(bool fp8);
+
+// Retrieval scorer (k_retrieval_tc.cu): one head, d a multiple of 64 up to
+// kRetrievalMaxDim, bf16, no causal mask.  The filter mode accumulates p.cnt
+// with global atomics and the per-query histogram ghist [T, nb] (zero both
+// first) shared by all CTAs that scan a query.
+cudaError_t launch_retrieval_tc(int mode, const CUtensorMap& q_map, const CUtensorMap& c_map,
+                                const ScoreParams& p, int dim, int relu, int* ghist,
+                                int num_sms, cudaStream_t stream);
+size_t retrieval_tc_smem_bytes(int mode, int nb);
 
 struct SampleStatsParams {
   const float* scores;     // [T, ld] sample scores (-inf = invisible)

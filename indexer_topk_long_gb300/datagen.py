@@ -271,3 +271,26 @@ def retrieval_queries(n: int = 1024, d: int = 768, n_centroids: int = 4096,
     rng = _rng(seed, 13)
     pick = rng.integers(0, n_centroids, size=n)
     return (np.float32(0.3) * cents[pick] + rng.standard_normal((n, d), dtype=np.float32)).astype(np.float32)
+
+
+def retrieval_inputs_torch(n_corpus: int = 8388608, n_queries: int = 1024, d: int = 768,
+                           n_centroids: int = 4096, seed: int = DEFAULT_SEED, device="cuda"):
+    """The retrieval workload generated on a device with a seeded torch
+    generator (a 12.9 GB corpus is impractical to draw with numpy): corpus rows
+    0.3 * centroid + N(0, 1) over random centroids, queries 0.3 * c + N(0, 1)
+    near random centroids, both rounded to bf16.  Returns (queries, corpus) as
+    bf16 tensors on ``device``; copy them to the host to feed the oracle."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    cents = torch.randn((n_centroids, d), generator=g, device=device)
+    corpus = torch.empty((n_corpus, d), dtype=torch.bfloat16, device=device)
+    step = 1 << 20
+    for r0 in range(0, n_corpus, step):
+        r1 = min(n_corpus, r0 + step)
+        a = torch.randint(0, n_centroids, (r1 - r0,), generator=g, device=device)
+        x = torch.randn((r1 - r0, d), generator=g, device=device)
+        corpus[r0:r1] = (0.3 * cents[a] + x).to(torch.bfloat16)
+    pick = torch.randint(0, n_centroids, (n_queries,), generator=g, device=device)
+    queries = (0.3 * cents[pick] + torch.randn((n_queries, d), generator=g, device=device)).to(torch.bfloat16)
+    return queries, corpus
