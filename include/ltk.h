@@ -83,6 +83,12 @@ typedef enum { LTK_BF16 = 0, LTK_FP8_E4M3 = 1 } ltk_dtype;
  *   rescue_rows     queries recomputed concurrently when a candidate list
  *                   overflows (each holds a max_S fp32 score row); 0 = 16.
  *   enable_host_io  1 also allocates device staging for ltk_indexer_topk_host.
+ *   debug_flags     0 in normal use.  Bit 0 (tests of failure handling): the
+ *                   Filter kernel's producer issues no key-tile loads, so its
+ *                   bounded waits expire (about 2 s), the kernel records
+ *                   LTK_ERR_TIMEOUT, releases its resources and returns; the
+ *                   outputs are then undefined and ltk_get_stats reports the
+ *                   status.
  */
 typedef struct {
   int heads;
@@ -101,6 +107,7 @@ typedef struct {
   int enable_decoupled;
   int rescue_rows;
   int enable_host_io;
+  int debug_flags;
 } ltk_config;
 
 typedef struct ltk_handle ltk_handle;

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (t0 + 4 * j) * kTcHeads, qbar);
         int issued[Sh::kStages];
         for (int s = 0; s < Sh::kStages; ++s) issued[s] = -1;
-        for (int i = 0; i < n_tiles; ++i) {
+        for (int i = 0; i < (p.skip_key_loads ? 0 : n_tiles); ++i) {
           const int s = i % Sh::kStages;
           if (i >= Sh::kStages &&
               !mbar_wait(smem_u32(&ctrl->k_empty[s]), ((i / Sh::kStages) - 1) & 1, abort_flag,

@@ -120,6 +120,7 @@ ltk_status validate_config(const ltk_config* c) {
   if (c->dtype != LTK_BF16 && c->dtype != LTK_FP8_E4M3) return LTK_ERR_ARG;
   if (c->sample_size < 0 || c->sample_size > kMaxSample) return LTK_ERR_ARG;
   if (c->cand_cap < 0 || c->refresh_interval < 0 || c->rescue_rows < 0) return LTK_ERR_ARG;
+  if (c->debug_flags & ~1) return LTK_ERR_ARG;
   if (!is_pow2(c->n_bins) || c->n_bins < 32) return LTK_ERR_ARG;
   if (is_retrieval(c)) {
     if (c->dtype != LTK_BF16 || c->causal || c->dim % 64 != 0 || c->dim > kRetrievalMaxDim ||
@@ -356,6 +357,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   fp.nb = c.n_bins;
   fp.k = a.k;
   fp.refresh_interval = c.refresh_interval;
+  fp.skip_key_loads = (c.debug_flags & 1) ? 1 : 0;
   fp.status = h->status;
   if (is_retrieval(&c)) {
     LTK_CUDA(cudaMemsetAsync(h->cnt, 0, static_cast<size_t>(a.T) * sizeof(int), st));

@@ -346,6 +346,7 @@ struct ScoreParams {
   int nb;
   int k;
   int refresh_interval;
+  int skip_key_loads;      // failure-handling tests: the producer issues no key tiles
   // Dense output
   float* dense;            // [T, ld]
   long long ld;

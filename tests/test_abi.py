@@ -47,7 +47,7 @@ def test_workspace_sizing(ltk_lib):
 @pytest.mark.parametrize("field,value,status", [
     ("k", 0, 1), ("k", 8193, 1), ("max_S", 0, 1), ("max_S", 1 << 31, 1), ("n_bins", 100, 1),
     ("n_bins", 16, 1), ("dtype", 7, 1), ("sample_size", 20000, 1), ("heads", 32, 6),
-    ("dim", 64, 6), ("relu", 0, 6), ("n_bins", 1024, 6),
+    ("dim", 64, 6), ("relu", 0, 6), ("n_bins", 1024, 6), ("debug_flags", 2, 1),
 ])
 def test_invalid_configs_rejected_on_host(ltk_lib, field, value, status):
     cfg = _cfg(**{field: value})
