@@ -157,6 +157,41 @@ __device__ __forceinline__ void refresh_threshold(const int* hist, int nb, int k
   }
 }
 
+// Same result as refresh_threshold, for a histogram row in global memory
+// (shared by the CTAs that split a query's keys): the warp fetches 16 segments
+// at a time with independent loads, so one L2 round trip covers 512 bins.
+__device__ __forceinline__ void refresh_threshold_global(const int* grow, int nb, int k,
+                                                         volatile int* theta, int lane) {
+  const int cur = *theta;
+  int run = 0;
+  for (int top0 = nb; top0 > cur; top0 -= 32 * 16) {
+    int v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int b = top0 - 1 - lane - 32 * j;
+      v[j] = b >= 0 ? __ldcg(grow + b) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int top = top0 - 32 * j;
+      if (top <= cur || top <= 0) return;
+      int cum = v[j];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+        if (lane >= o) cum += n;
+      }
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, run + cum >= k);
+      if (m != 0) {
+        const int th = top - 1 - (__ffs(m) - 1);
+        if (lane == 0 && th > cur) *theta = th;
+        return;
+      }
+      run += __shfl_sync(0xFFFFFFFFu, cum, 31);
+    }
+  }
+}
+
 template <int MODE, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap q_map,
@@ -176,7 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int t0 = blockIdx.x * kTcQPB;
+  // work unit: a whole query block, or one key range of a split query block
+  int qb = blockIdx.x, split = 0, nsplit = 1;
+  if (static_cast<int>(blockIdx.x) >= p.b_full && p.s_last > 1) {
+    const int u = blockIdx.x - p.b_full;
+    qb = p.b_full + u / p.s_last;
+    split = u % p.s_last;
+    nsplit = p.s_last;
+  }
+  const bool shared_query = nsplit > 1;   // other CTAs scan other keys of these queries
+  const int t0 = qb * kTcQPB;
   const int nq = min(kTcQPB, p.T - t0);
 
   // Keys to scan: up to the largest position in the block when causal.
@@ -187,7 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     last_row = min(static_cast<long long>(mp) + 1, p.rows);
     if (last_row < 0) last_row = 0;
   }
-  const int n_tiles = static_cast<int>((last_row + kTile - 1) / kTile);
+  const int block_tiles = static_cast<int>((last_row + kTile - 1) / kTile);
+  const int per_split = (block_tiles + nsplit - 1) / nsplit;
+  const int tile_lo = split * per_split;
+  const int n_tiles = max(0, min(per_split, block_tiles - tile_lo));
 
   // ---- setup: weights, per-query state, histogram, barriers, TMEM
   // Weights in the epilogue's order: entry [ql][c][2r + i] holds head
@@ -262,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(fb, Sh::kKStage);
           for (int c = 0; c < Sh::kChunks; ++c)
             tma_load_2d(s_k + s * Sh::kKStage + c * Sh::kKChunkBytes, &k_map, c * Sh::kBoxCols,
-                        i * kTile, fb);
+                        (tile_lo + i) * kTile, fb);
           issued[s] = i;
         }
         if (*abort_flag) {
@@ -326,9 +373,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (done - last >= p.refresh_interval) {
               last = done;
-              for (int ql = 0; ql < nq; ++ql)
-                refresh_threshold(hist + ql * p.nb, p.nb, p.k,
-                                  reinterpret_cast<volatile int*>(&ctrl->theta[ql]), lane);
+              for (int ql = 0; ql < nq; ++ql) {
+                if (shared_query) {
+                  // move this CTA's new counts into the query's histogram over all
+                  // CTAs, then take the threshold from those counts
+                  int* grow = p.ghist + static_cast<size_t>(t0 + ql) * p.nb;
+                  for (int b = lane; b < p.nb; b += 32) {
+                    const int cnt_b = atomicExch(&hist[ql * p.nb + b], 0);
+                    if (cnt_b != 0) atomicAdd(&grow[b], cnt_b);
+                  }
+                  __syncwarp();
+                  refresh_threshold_global(grow, p.nb, p.k,
+                                           reinterpret_cast<volatile int*>(&ctrl->theta[ql]), lane);
+                } else {
+                  refresh_threshold(hist + ql * p.nb, p.nb, p.k,
+                                    reinterpret_cast<volatile int*>(&ctrl->theta[ql]), lane);
+                }
+              }
             } else {
               __nanosleep(1000);
               bool expired = globaltimer_ns() - t_prog > kWaitLimitNs;
@@ -388,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc_empty0 = smem_u32(&ctrl->acc_empty[0]);
       const uint32_t tq0 = tmem + lane_base + qh * kTcHeads;
       for (int i = 0; i < n_tiles; ++i) {
-        const int key = i * kTile + row;
+        const int key = (tile_lo + i) * kTile + row;
         const bool key_ok = key < rows_i;
         float kscale = 1.f;
         if constexpr (FP8) kscale = key_ok ? p.k_scale[key] : 0.f;
@@ -432,7 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (m != 0) {
               const int leader = __ffs(m) - 1;
               int base = 0;
-              if (lane == leader) base = atomicAdd(&ctrl->cnt[ql], __popc(m));
+              if (lane == leader)
+                base = shared_query ? atomicAdd(&p.cnt[t0 + ql], __popc(m))
+                                    : atomicAdd(&ctrl->cnt[ql], __popc(m));
               base = __shfl_sync(0xFFFFFFFFu, base, leader);
               if (pass) {
                 const int slot = base + __popc(m & ((1u << lane) - 1u));
@@ -457,15 +520,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
   if constexpr (MODE == kModeFilter) {
-    if (tid < nq) p.cnt[t0 + tid] = ctrl->cnt[tid];
+    if (tid < nq && !shared_query) p.cnt[t0 + tid] = ctrl->cnt[tid];
   }
 }
 
 template <int MODE, bool FP8>
 cudaError_t launch_one(const CUtensorMap& qm, const CUtensorMap& km, const ScoreParams& p,
                        cudaStream_t stream) {
-  const int grid = (p.T + kTcQPB - 1) / kTcQPB;
-  if (grid == 0) return cudaSuccess;
+  const int t_blocks = (p.T + kTcQPB - 1) / kTcQPB;
+  if (t_blocks == 0) return cudaSuccess;
+  const int grid = p.b_full + (t_blocks - p.b_full) * (p.s_last > 1 ? p.s_last : 1);
   const size_t smem = smem_bytes<FP8>(MODE == kModeFilter ? p.nb : 0);
   static size_t configured = 0;
   if (configured < smem) {

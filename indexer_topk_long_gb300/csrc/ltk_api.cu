@@ -38,7 +38,7 @@ struct ltk_handle {
   unsigned long long* cand = nullptr;  // [max_T, cap]
   int* cnt = nullptr;                  // [max_T]
   int* ovf = nullptr;                  // [2 + max_T]: count, next, list
-  int* ghist = nullptr;                // [max_T, n_bins] per-query histograms shared by CTAs (retrieval)
+  int* ghist = nullptr;                // [max_T, n_bins] per-query histograms shared by CTAs
   float* rescue_scratch = nullptr;     // [rescue_rows, max_S]
   float* dense = nullptr;              // [max_T, max_S] (decoupled baseline)
   int* status = nullptr;               // [1]
@@ -95,13 +95,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
-int derived_cap(int k, long long max_S) {
+int derived_cap(int k, long long max_S, int max_T) {
   // Expected candidates of a streaming threshold grow like k * (1 + ln(S / k));
   // the default keeps a 1.5x margin over k * (4 + ln(S / k)) plus 2048 records
-  // (small k starts from a loose sample threshold), never above S.
+  // (small k starts from a loose sample threshold), never above S (rounded).
   const double ratio = static_cast<double>(max_S) / static_cast<double>(k);
   const double est = k * (4.0 + std::log(ratio > 1.0 ? ratio : 1.0)) * 1.5 + 2048.0;
   long long cap = round_up(static_cast<long long>(est), 1024);
+  // Small chunks (decode) split a query's keys over many CTAs, where the shared
+  // threshold tightens in coarser steps; memory is no constraint there, so the
+  // capacity grows to a budget of 2^27 records spread over max_T queries.
+  const long long budget = round_up((1ll << 27) / (max_T > 0 ? max_T : 1), 1024);
+  if (cap < budget) cap = budget;
   const long long s_cap = round_up(max_S, 1024);
   if (cap > s_cap) cap = s_cap;
   if (cap < k) cap = k;
@@ -142,7 +147,7 @@ struct Sizes {
 Sizes compute_sizes(const ltk_config* c) {
   Sizes s{};
   s.elem = c->dtype == LTK_FP8_E4M3 ? 1 : 2;
-  s.cap = c->cand_cap > 0 ? c->cand_cap : derived_cap(c->k, c->max_S);
+  s.cap = c->cand_cap > 0 ? c->cand_cap : derived_cap(c->k, c->max_S, c->max_T);
   const int ss = c->sample_size > 0 ? c->sample_size : (3 * c->k > kMaxSample ? kMaxSample : 3 * c->k);
   s.n_pad_max = static_cast<int>(round_up(kMaxSample > ss ? kMaxSample : ss, kTile));
   s.rescue_rows = c->rescue_rows > 0 ? c->rescue_rows : 16;
@@ -154,7 +159,7 @@ Sizes compute_sizes(const ltk_config* c) {
   b += static_cast<unsigned long long>(s.n_pad_max) * 4 * 2;            // scales + ids
   b += kMaxSample * 4ull;                             // random sample ids
   b += T * 4 * 4;                                     // s_min, delta, theta0, cnt
-  if (is_retrieval(c)) b += T * static_cast<unsigned long long>(c->n_bins) * 4;   // shared histograms
+  b += T * static_cast<unsigned long long>(c->n_bins) * 4;   // per-query histograms shared by CTAs
   b += T * static_cast<unsigned long long>(s.cap) * 8;  // candidate lists
   b += (T + 2) * 4;                                   // overflow list
   b += static_cast<unsigned long long>(s.rescue_rows) * S * 4;   // rescue rows
@@ -279,6 +284,42 @@ cudaError_t launch_scorer(const ltk_handle* h, int mode, const CUtensorMap& qm, 
   return launch_score_tc(mode, c.dtype == LTK_FP8_E4M3, qm, km, p, st);
 }
 
+// Work split of the indexer scorer over (query block, key range) units.  Whole
+// waves of query blocks stay unsplit; the query blocks of a partial last wave
+// (or of a chunk smaller than one wave, e.g. decode) are split along the keys
+// into s_last ranges, chosen so that the split units fill the SMs best, with
+// at least 64 key tiles per range.
+void plan_split(int T, long long S, int num_sms, int* b_full, int* s_last) {
+  const int t_blocks = (T + kTcQPB - 1) / kTcQPB;
+  const long long tiles = (S + kTile - 1) / kTile;
+  const int max_s = static_cast<int>(tiles / 64 > 1 ? (tiles / 64 < 64 ? tiles / 64 : 64) : 1);
+  *b_full = t_blocks;
+  *s_last = 1;
+  if (t_blocks == 0 || max_s <= 1) return;
+  const int rem = t_blocks % num_sms;
+  if (t_blocks < num_sms) {
+    *b_full = 0;
+    int sl = num_sms / t_blocks;
+    *s_last = sl < max_s ? sl : max_s;
+    if (*s_last < 1) *s_last = 1;
+    return;
+  }
+  if (rem == 0) return;
+  double best = 1.0;
+  int best_s = 1;
+  for (int sl = 2; sl <= 8 && sl <= max_s; ++sl) {
+    const double cost = static_cast<double>((rem * sl + num_sms - 1) / num_sms) / sl;
+    if (cost < best - 0.02) {
+      best = cost;
+      best_s = sl;
+    }
+  }
+  if (best_s > 1) {
+    *b_full = t_blocks - rem;
+    *s_last = best_s;
+  }
+}
+
 // Rows of q seen by TMA: [T * H, d].
 unsigned long long q_rows(const ltk_config& c, int T) {
   return static_cast<unsigned long long>(T) * c.heads;
@@ -333,6 +374,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   sp.dense = h->samp_scores;
   sp.ld = n_pad;
   sp.status = h->status;
+  plan_split(a.T, n_pad, h->num_sms, &sp.b_full, &sp.s_last);
   LTK_CUDA(launch_scorer(h, kModeDense, q_map, ks_map, sp, st));
   SampleStatsParams stp{h->samp_scores, n_pad, n_pad, a.T, a.k, c.n_bins, h->s_min, h->delta, h->theta0};
   LTK_CUDA(launch_sample_stats(stp, st));
@@ -358,7 +400,16 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   fp.k = a.k;
   fp.refresh_interval = c.refresh_interval;
   fp.skip_key_loads = (c.debug_flags & 1) ? 1 : 0;
+  fp.ghist = h->ghist;
   fp.status = h->status;
+  plan_split(a.T, a.S, h->num_sms, &fp.b_full, &fp.s_last);
+  if (!is_retrieval(&c) && fp.s_last > 1) {
+    // split query blocks count and build histograms in global memory
+    const size_t t_first = static_cast<size_t>(fp.b_full) * kTcQPB;
+    const size_t n = static_cast<size_t>(a.T) - t_first;
+    LTK_CUDA(cudaMemsetAsync(h->cnt + t_first, 0, n * sizeof(int), st));
+    LTK_CUDA(cudaMemsetAsync(h->ghist + t_first * c.n_bins, 0, n * c.n_bins * sizeof(int), st));
+  }
   if (is_retrieval(&c)) {
     LTK_CUDA(cudaMemsetAsync(h->cnt, 0, static_cast<size_t>(a.T) * sizeof(int), st));
     LTK_CUDA(cudaMemsetAsync(h->ghist, 0, static_cast<size_t>(a.T) * c.n_bins * sizeof(int), st));
@@ -483,7 +534,7 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
   step(alloc(&h->s_min, T * 4));
   step(alloc(&h->delta, T * 4));
   step(alloc(&h->theta0, T * 4));
-  if (is_retrieval(cfg)) step(alloc(&h->ghist, T * static_cast<unsigned long long>(cfg->n_bins) * 4));
+  step(alloc(&h->ghist, T * static_cast<unsigned long long>(cfg->n_bins) * 4));
   step(alloc(&h->cand, T * static_cast<unsigned long long>(h->cap) * 8));
   step(alloc(&h->cnt, T * 4));
   step(alloc(&h->ovf, (T + 2) * 4));
@@ -644,6 +695,7 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   sp.dense = h->dense;
   sp.ld = S;
   sp.status = h->status;
+  plan_split(T, S, h->num_sms, &sp.b_full, &sp.s_last);
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
   LTK_CUDA(launch_scorer(h, kModeDense, q_map, k_map, sp, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[2], st));
@@ -800,6 +852,8 @@ extern "C" ltk_status ltk_decoupled_topk_noalloc(int dtype, int causal, const vo
   sp.dense = scores;
   sp.ld = S;
   sp.status = nullptr;
+  sp.b_full = (T + kTcQPB - 1) / kTcQPB;
+  sp.s_last = 1;
   LTK_CUDA(launch_score_tc(kModeDense, fp8, q_map, k_map, sp, st));
   RowTopkParams rp{scores, S, causal ? positions : nullptr, T, S, causal ? 1 : 0, k, out_idx,
                    out_score, nullptr};

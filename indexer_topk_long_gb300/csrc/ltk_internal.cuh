@@ -347,6 +347,13 @@ struct ScoreParams {
   int k;
   int refresh_interval;
   int skip_key_loads;      // failure-handling tests: the producer issues no key tiles
+  // Work split (indexer scorer): CTAs [0, b_full) each own one query block and
+  // all of its keys; the remaining query blocks are each split into s_last key
+  // ranges scanned by s_last CTAs, which append with global atomics to cnt and
+  // drain their histograms into ghist [T, nb] (both zeroed before the launch).
+  int b_full;
+  int s_last;
+  int* ghist;
   // Dense output
   float* dense;            // [T, ld]
   long long ld;

@@ -165,3 +165,16 @@ def test_empty_chunk_and_k_larger_than_visible():
     op(d["q"][:0], d["w"][:0], d["k_cache"], d["positions"][:0], k=16, out=(e_idx, e_sc))
     torch.cuda.synchronize()
     op.close()
+
+
+@pytest.mark.parametrize("T,S,integer", [(1, 300000, True), (5, 300000, False), (16, 200003, True)])
+def test_decode_small_chunks_split_over_keys(T, S, integer):
+    """Few queries against a long cache (decode-like): the query block's keys are
+    split over many CTAs that share the candidate count and histogram."""
+    inp = datagen.make_indexer_inputs(T=T, first_pos=S - T, S=S, integer=integer, seed=40 + T)
+    idx, sc, st = _run(inp, 2048)
+    assert st["n_overflow"] == 0
+    if integer:
+        check_exact(inp, idx, sc, 2048)
+    else:
+        check_tolerant(inp, idx, sc, 2048)
