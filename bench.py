@@ -60,6 +60,8 @@ def parse_args():
                     help="queries of the chunk the CPU oracle baseline scores")
     ap.add_argument("--ref-queries", type=int, default=2,
                     help="queries per step of the reference (oracle) arm")
+    ap.add_argument("--k", type=int, default=0,
+                    help="retrieval workload: k (default 1000; the pages sweep 1024..8192)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decoupled", action="store_true")
@@ -265,7 +267,7 @@ def run_reference(args):
 
 
 RETRIEVAL = dict(T=1024, N=8388608, d=768, k=1000, sample=3000)
-RETRIEVAL_METRIC = "scored query-vector pairs/s, vector retrieval 1024 x 8.4M, d=768, k=1000 (1 GB300)"
+RETRIEVAL_METRIC = "scored query-vector pairs/s, vector retrieval 1024 x 8.4M, d=768 (1 GB300)"
 
 
 def run_retrieval(args):
@@ -280,7 +282,10 @@ def run_retrieval(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-    R = RETRIEVAL
+    R = dict(RETRIEVAL)
+    if args.k:
+        R["k"] = args.k
+        R["sample"] = min(3 * args.k, 16384)
     T = args.queries or R["T"]
     q, c = datagen.retrieval_inputs_torch(R["N"], T, R["d"], seed=20260715 + rank, device=dev)
     w = torch.ones((T, 1), dtype=torch.float32, device=dev)

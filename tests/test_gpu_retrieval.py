@@ -74,3 +74,14 @@ def test_retrieval_overflow_rescued():
     ref_idx, ref_sc = orc.retrieval_topk(qb, cb, 300)
     np.testing.assert_array_equal(out["idx"], ref_idx)
     np.testing.assert_array_equal(out["sc"], ref_sc)
+
+
+@pytest.mark.parametrize("k", [2048, 4096, 8192])
+def test_retrieval_large_k(k):
+    """k from 1024 to 8192, the range of the pages' retrieval comparison."""
+    qb, cb = _inputs(48, 100003, 768, seed=k)
+    out = _run(qb, cb, k, enable_decoupled=1)
+    assert out["stats"]["n_overflow"] == 0 and out["dec_equal"]
+    S = orc.bf16_to_f64(qb) @ orc.bf16_to_f64(cb).T
+    for t in range(0, 48, 5):
+        check_row_tolerant(out["idx"][t], out["sc"][t], S[t], k, where=f"query {t}")
