@@ -505,6 +505,19 @@ def main():
                                     "decoupled": 4.0 * pairs_step / wl.T},
     }
 
+    # ---- LiteDSA packing of the chunk's output (groups of 8 neighbouring queries)
+    from indexer_topk_long_gb300 import litedsa_pack
+    litedsa_pack(out_idx, 8)
+    torch.cuda.synchronize()
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    _, lens, _ = litedsa_pack(out_idx, 8)
+    l1.record(stream)
+    torch.cuda.synchronize()
+    line["litedsa"] = {"group": 8, "ms": l0.elapsed_time(l1),
+                       "kv_rows_packed": int(lens.sum().item()), "kv_rows_per_query_lists": wl.T * k,
+                       "kv_row_ratio": float(lens.sum().item()) / (wl.T * k)}
+
     # ---- end to end through the host-buffer C-ABI call
     if not args.no_e2e:
         sample = op.make_sample(prev_idx, wl.S, 3 * k).cpu().pin_memory()

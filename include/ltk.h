@@ -262,6 +262,25 @@ ltk_status ltk_decoupled_topk_noalloc(int dtype, int causal, const void* q, cons
                                       const int* positions, int T, long long S, int k,
                                       int* out_idx, float* out_score, void* stream);
 
+/*
+ * LiteDSA candidate packing (LiteTopK arXiv abstract: LiteDSA packs the
+ * overlapping candidates of neighbouring query tokens into a shared key/value
+ * list for joint attention, with per-query masks that keep each token's own
+ * top-k membership).  Consecutive queries form groups of `group`; for group g
+ * (queries g*group .. g*group+group-1, the last group may be short):
+ *   union_idx  device int32 [ceil(T/group), group*k]: the ascending set union
+ *              of the group's valid (>= 0) indices, padded with -1;
+ *   union_len  device int32 [ceil(T/group)]: number of valid union entries;
+ *   masks      device uint32 [T, ceil(group*k/32)]: bit j of query t's row is
+ *              set iff union entry j of t's group is one of t's indices.
+ * topk_idx is device int32 [T, k] (e.g. ltk_indexer_topk's out_idx; a row
+ * holds distinct indices, -1 = empty slot).  No handle, no allocation.
+ * group in [1, 256]; group*k <= 16384 and the group's shared-memory footprint
+ * (sorted keys + masks) <= 200 KB, else LTK_ERR_UNSUPPORTED.
+ */
+ltk_status ltk_litedsa_pack(const int* topk_idx, int T, int k, int group, int* union_idx,
+                            int* union_len, unsigned int* masks, void* stream);
+
 /* Statistics of the last compute call (synchronises its stream). */
 ltk_status ltk_get_stats(ltk_handle* h, ltk_stats* out);
 

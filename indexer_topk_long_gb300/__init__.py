@@ -3,4 +3,4 @@
 The compute path lives in the CUDA library ``libltk.so`` (sources in ``csrc/``,
 C ABI in ``include/ltk.h``); ``ltk`` is a thin ctypes binding over it.
 """
-from .ltk import IndexerTopK, LtkError, load_library, library_path  # noqa: F401
+from .ltk import IndexerTopK, LtkError, litedsa_pack, load_library, library_path  # noqa: F401

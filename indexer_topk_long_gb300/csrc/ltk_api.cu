@@ -709,6 +709,18 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   return LTK_OK;
 }
 
+ltk_status ltk_litedsa_pack(const int* topk_idx, int T, int k, int group, int* union_idx,
+                            int* union_len, unsigned int* masks, void* stream) {
+  if (T < 0 || k < 1 || group < 1 || group > 256) return LTK_ERR_ARG;
+  if (static_cast<long long>(group) * k > litedsa_max_entries()) return LTK_ERR_UNSUPPORTED;
+  if (litedsa_smem_bytes(group, k) > kLitedsaMaxSmem) return LTK_ERR_UNSUPPORTED;
+  if (T == 0) return LTK_OK;
+  if (!topk_idx || !union_idx || !union_len || !masks) return LTK_ERR_ARG;
+  LTK_CUDA(launch_litedsa_pack(topk_idx, T, k, group, union_idx, union_len, masks,
+                               static_cast<cudaStream_t>(stream)));
+  return LTK_OK;
+}
+
 ltk_status ltk_get_stats(ltk_handle* h, ltk_stats* out) {
   if (h == nullptr || out == nullptr) return LTK_ERR_ARG;
   std::memset(out, 0, sizeof(*out));

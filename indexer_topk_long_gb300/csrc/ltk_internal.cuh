@@ -461,6 +461,15 @@ struct RescueParams {
   float* out_score;
 };
 
+// LiteDSA packing (k_litedsa.cu): per group of G queries, the ascending union
+// of their selected indices and per-query membership masks.  Needs
+// G * k <= litedsa_max_entries() and litedsa_smem_bytes(G, k) <= kLitedsaMaxSmem.
+constexpr size_t kLitedsaMaxSmem = 200 * 1024;
+int litedsa_max_entries();
+size_t litedsa_smem_bytes(int G, int k);
+cudaError_t launch_litedsa_pack(const int* topk, int T, int k, int G, int* union_idx, int* union_len,
+                                uint32_t* masks, cudaStream_t stream);
+
 // Select stage, decoupled baseline selection and overflow rescue (k_select.cu).
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
 cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream);

@@ -67,6 +67,7 @@ _SIGS = {
     "ltk_decoupled_topk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _LL, _I, _P, _P, _P]),
     "ltk_get_stats": (_I, [_P, ctypes.POINTER(Stats)]),
     "ltk_decoupled_topk_noalloc": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _I, _LL, _I, _P, _P, _P]),
+    "ltk_litedsa_pack": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
 }
 
 _LIB = None
@@ -130,6 +131,25 @@ def workspace_bytes(cfg: Config) -> int:
     out = ctypes.c_ulonglong(0)
     _check(lib.ltk_workspace_bytes(ctypes.byref(cfg), ctypes.byref(out)), "ltk_workspace_bytes")
     return out.value
+
+
+def litedsa_pack(topk_idx, group: int, stream=None):
+    """LiteDSA packing of a [T, k] int32 CUDA tensor of selected indices.
+
+    Returns (union [ceil(T/group), group*k] int32, lengths [ceil(T/group)] int32,
+    masks [T, ceil(group*k/32)] int32 holding the uint32 bit patterns)."""
+    import torch
+    lib = load_library()
+    T, k = int(topk_idx.shape[0]), int(topk_idx.shape[1])
+    n_groups = (T + group - 1) // group
+    words = (group * k + 31) // 32
+    dev = topk_idx.device
+    union = torch.empty((n_groups, group * k), dtype=torch.int32, device=dev)
+    lens = torch.empty((n_groups,), dtype=torch.int32, device=dev)
+    masks = torch.empty((T, words), dtype=torch.int32, device=dev)
+    _check(lib.ltk_litedsa_pack(_ptr(topk_idx), T, k, group, _ptr(union), _ptr(lens), _ptr(masks),
+                                _stream_handle(stream)), "ltk_litedsa_pack")
+    return union, lens, masks
 
 
 class IndexerTopK:
