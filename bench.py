@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ltk", "reference"], default="ltk")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["retrieval"], default="1m")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["retrieval", "decode"], default="1m")
     ap.add_argument("--dtype", choices=["bf16", "fp8"], default="bf16")
     ap.add_argument("--queries", type=int, default=0,
                     help="run only the first N queries of the chunk (profiling a single wave)")
@@ -388,12 +388,66 @@ def run_retrieval(args):
     return 0
 
 
+DECODE_METRIC = "decode: scored query-key pairs/s and ms per call, T new tokens at 1M ctx, k=2048 (1 GB300)"
+
+
+def run_decode(args):
+    """Decode / small-T: T queries (default 1) at the end of a 1M-token cache,
+    previous-step sample; the key range is split over the GPU."""
+    import numpy as np
+    import torch
+    from indexer_topk_long_gb300 import IndexerTopK, datagen
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    T = args.queries or 1
+    S = 1 << 20
+    keys = datagen.keys_fp32(S, 128, 20260715 + rank)
+    inp = datagen.make_indexer_inputs(T, S - T, S, dtype=args.dtype, seed=20260715 + rank, keys=keys)
+    d = to_dev(inp, torch, dev)
+    op = IndexerTopK(max_T=T, max_S=S, k=2048, dtype=args.dtype)
+    out = (torch.empty((T, 2048), dtype=torch.int32, device=dev),
+           torch.empty((T, 2048), dtype=torch.float32, device=dev))
+    first = op(d["q"], d["w"], d["k_cache"], d["positions"], k=2048, q_scale=d["q_scale"], k_scale=d["k_scale"])
+    sample = op.make_sample(first[0], S, 6144)
+    stream = torch.cuda.current_stream()
+    step = lambda: op(d["q"], d["w"], d["k_cache"], d["positions"], k=2048, prev_topk=sample,
+                      q_scale=d["q_scale"], k_scale=d["k_scale"], out=out)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    op.set_timing(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st = op.stats()
+    ms = e0.elapsed_time(e1) / args.steps
+    pairs = st["visible_pairs"]
+    line = {"metric": DECODE_METRIC, "value": world * pairs / (ms * 1e-3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+            "data": "synthetic (seeded hot-key/topic generator)",
+            "config": {"workload": f"decode: T={T} queries at positions {S - T}..{S - 1}, S={S}, H=64, "
+                                   f"d=128, k=2048, previous-step sample; keys split over the GPU"},
+            "stages_ms": {"sample": st["ms_sample"], "filter": st["ms_filter"], "select": st["ms_select"]},
+            "candidates_per_query": st["cand_written"] / T, "n_overflow": st["n_overflow"]}
+    op.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "retrieval":
         return run_retrieval(args)
+    if args.workload == "decode":
+        return run_decode(args)
     import numpy as np
     import torch
     from indexer_topk_long_gb300 import IndexerTopK
