@@ -59,8 +59,8 @@ typedef enum { LTK_BF16 = 0, LTK_FP8_E4M3 = 1 } ltk_dtype;
 
 /*
  * Handle configuration (fixed at ltk_create).
- *   heads, dim      H and d of q[T,H,d] and k[S,d].  The tensor-core path
- *                   implements H = 64, d = 128 (the indexer shape).
+ *   heads, dim      H and d of q[T,H,d] and k[S,d] (see engine for the shapes
+ *                   each kernel serves).
  *   dtype           LTK_BF16, or LTK_FP8_E4M3 with per-token fp32 scales
  *                   (q_scale[T], k_scale[S]; the value is code * scale).
  *   relu, causal    1 for the indexer score (ReLU per head, key s visible iff
@@ -83,6 +83,12 @@ typedef enum { LTK_BF16 = 0, LTK_FP8_E4M3 = 1 } ltk_dtype;
  *   rescue_rows     queries recomputed concurrently when a candidate list
  *                   overflows (each holds a max_S fp32 score row); 0 = 16.
  *   enable_host_io  1 also allocates device staging for ltk_indexer_topk_host.
+ *   engine          0 (auto): the tensor-core kernels where the shape allows
+ *                   (H = 64 and d = 128 with ReLU; or H = 1, bf16, no mask),
+ *                   otherwise the CUDA-core kernel; 1: tensor cores only;
+ *                   2: the CUDA-core kernel with the fused affine bin map
+ *                   (any 1 <= H <= 128, d a multiple of 8 -- of 16 for
+ *                   e4m3 -- up to 4096, H * d * 4 + n_bins * 4 <= 100 KB).
  *   debug_flags     0 in normal use.  Bit 0 (tests of failure handling): the
  *                   Filter kernel's producer issues no key-tile loads, so its
  *                   bounded waits expire (about 2 s), the kernel records
@@ -107,6 +113,7 @@ typedef struct {
   int enable_decoupled;
   int rescue_rows;
   int enable_host_io;
+  int engine;
   int debug_flags;
 } ltk_config;
 

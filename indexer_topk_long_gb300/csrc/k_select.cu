@@ -472,10 +472,49 @@ __device__ void rescue_row_scores_one_head(const RescueParams& p, int t, int V, 
   __syncthreads();
 }
 
+// Any head count and dimension (the CUDA-core engine's shapes): one thread per
+// key, heads one after another, the key row re-read from cache per head.
+__device__ void rescue_row_scores_generic(const RescueParams& p, int t, int V, float* row,
+                                          float* qf, float* wf) {
+  const int H = p.heads, d = p.dim;
+  const size_t qoff = static_cast<size_t>(t) * H * d;
+  for (int i = threadIdx.x; i < H * d; i += blockDim.x) {
+    qf[i] = p.fp8 ? e4m3_value(static_cast<const uint8_t*>(p.q)[qoff + i])
+                  : __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p.q)[qoff + i]) << 16);
+  }
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    float wv = p.w[static_cast<size_t>(t) * H + h];
+    if (p.fp8) wv = __fmul_rn(wv, p.q_scale[t]);
+    wf[h] = wv;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < V; s += blockDim.x) {
+    float I = 0.f;
+    for (int h = 0; h < H; ++h) {
+      const float* qh = qf + h * d;
+      float acc = 0.f;
+      for (int i = 0; i < d; ++i) {
+        const float kv = p.fp8 ? e4m3_value(static_cast<const uint8_t*>(p.k_cache)[static_cast<size_t>(s) * d + i])
+                               : __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(
+                                     p.k_cache)[static_cast<size_t>(s) * d + i]) << 16);
+        acc = __fmaf_rn(qh[i], kv, acc);
+      }
+      I = __fmaf_rn(p.relu ? fmaxf(acc, 0.f) : acc, wf[h], I);
+    }
+    if (p.fp8) I = __fmul_rn(I, p.k_scale[s]);
+    row[s] = I;
+  }
+  __syncthreads();
+}
+
 __device__ void rescue_row_scores(const RescueParams& p, int t, int V, float* row, float* qf,
                                   float* wf) {
-  if (p.heads == 1) {
+  if (p.heads == 1 && !p.fp8) {
     rescue_row_scores_one_head(p, t, V, row, qf);
+    return;
+  }
+  if (p.heads != kTcHeads || p.dim != kTcDim) {
+    rescue_row_scores_generic(p, t, V, row, qf, wf);
     return;
   }
   const int H = kTcHeads, d = kTcDim;
@@ -543,7 +582,7 @@ __global__ void __launch_bounds__(kRescueThreads) rescue_kernel(const RescuePara
   __shared__ long long sh[2];
   __shared__ int sh_int[2];
   __shared__ int s_slot;
-  __shared__ float wf[kTcHeads];
+  __shared__ float wf[128];
   float* qf = reinterpret_cast<float*>(rs_smem);   // [H*d] fp32, reused as output buffer later
   float* row = p.scratch + static_cast<size_t>(blockIdx.x) * p.scratch_ld;
   while (true) {
@@ -602,11 +641,11 @@ cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream) {
 
 cudaError_t launch_rescue(const RescueParams& p, int rescue_rows, cudaStream_t stream) {
   if (p.T <= 0 || rescue_rows <= 0) return cudaSuccess;
-  const size_t qbytes = static_cast<size_t>(kTcHeads) * kTcDim * sizeof(float);
+  const size_t qbytes = static_cast<size_t>(p.heads) * p.dim * sizeof(float);
   const size_t smem = qbytes > outbuf_bytes(p.k) ? qbytes : outbuf_bytes(p.k);
   static bool configured = false;
   if (!configured) {
-    const size_t mx = qbytes > outbuf_bytes(kMaxK) ? qbytes : outbuf_bytes(kMaxK);
+    const size_t mx = kCcMaxSmem > outbuf_bytes(kMaxK) ? kCcMaxSmem : outbuf_bytes(kMaxK);
     cudaError_t e = cudaFuncSetAttribute(rescue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(mx));
     if (e != cudaSuccess) return e;

@@ -114,8 +114,28 @@ int derived_cap(int k, long long max_S, int max_T) {
   return static_cast<int>(cap);
 }
 
-// One head, plain inner product: the vector-retrieval shape.
-bool is_retrieval(const ltk_config* c) { return c->heads == 1; }
+// Shapes each kernel serves.
+bool tc_shape(const ltk_config* c) {
+  return c->heads == kTcHeads && c->dim == kTcDim && c->relu == 1 &&
+         c->n_bins <= score_tc_max_bins(c->dtype == LTK_FP8_E4M3);
+}
+bool retrieval_shape(const ltk_config* c) {
+  return c->heads == 1 && c->dtype == LTK_BF16 && !c->causal && c->dim % 64 == 0 &&
+         c->dim <= kRetrievalMaxDim && c->n_bins <= kRetrievalMaxBins && (c->relu == 0 || c->relu == 1);
+}
+bool cc_shape(const ltk_config* c) {
+  const int elem = c->dtype == LTK_FP8_E4M3 ? 1 : 2;
+  return c->heads >= 1 && c->heads <= 128 && c->dim % 8 == 0 && c->dim <= 4096 &&
+         (c->dim * elem) % 16 == 0 && (c->relu == 0 || c->relu == 1) && c->n_bins <= 4096 &&
+         score_cc_smem_bytes(c->heads, c->dim, c->n_bins) <= kCcMaxSmem;
+}
+// The CUDA-core scorer runs when asked for, or when no tensor-core kernel
+// serves the shape.
+bool use_cc(const ltk_config* c) {
+  return c->engine == 2 || (c->engine == 0 && !tc_shape(c) && !retrieval_shape(c));
+}
+// One head on the tensor-core path: the vector-retrieval kernel.
+bool is_retrieval(const ltk_config* c) { return c->heads == 1 && !use_cc(c); }
 
 ltk_status validate_config(const ltk_config* c) {
   if (c == nullptr) return LTK_ERR_ARG;
@@ -127,14 +147,10 @@ ltk_status validate_config(const ltk_config* c) {
   if (c->cand_cap < 0 || c->refresh_interval < 0 || c->rescue_rows < 0) return LTK_ERR_ARG;
   if (c->debug_flags & ~1) return LTK_ERR_ARG;
   if (!is_pow2(c->n_bins) || c->n_bins < 32) return LTK_ERR_ARG;
-  if (is_retrieval(c)) {
-    if (c->dtype != LTK_BF16 || c->causal || c->dim % 64 != 0 || c->dim > kRetrievalMaxDim ||
-        c->n_bins > kRetrievalMaxBins || (c->relu != 0 && c->relu != 1))
-      return LTK_ERR_UNSUPPORTED;
-    return LTK_OK;
-  }
-  if (c->heads != kTcHeads || c->dim != kTcDim || c->relu != 1) return LTK_ERR_UNSUPPORTED;
-  if (c->n_bins > score_tc_max_bins(c->dtype == LTK_FP8_E4M3)) return LTK_ERR_UNSUPPORTED;
+  if (c->engine < 0 || c->engine > 2) return LTK_ERR_ARG;
+  if (c->engine == 1 && !tc_shape(c) && !retrieval_shape(c)) return LTK_ERR_UNSUPPORTED;
+  if (c->engine == 2 && !cc_shape(c)) return LTK_ERR_UNSUPPORTED;
+  if (c->engine == 0 && !tc_shape(c) && !retrieval_shape(c) && !cc_shape(c)) return LTK_ERR_UNSUPPORTED;
   return LTK_OK;
 }
 
@@ -274,11 +290,44 @@ ltk_status validate_call(const ltk_handle* h, const CallArgs& a) {
   return LTK_OK;
 }
 
-// The scorer for the handle's shape: the indexer kernel (H = 64, d = 128) or
-// the retrieval kernel (one head).
+// The scorer for the handle's shape: the tensor-core indexer kernel (H = 64,
+// d = 128), the tensor-core retrieval kernel (one head), or the CUDA-core
+// kernel (any other shape, or when asked for).
 cudaError_t launch_scorer(const ltk_handle* h, int mode, const CUtensorMap& qm, const CUtensorMap& km,
                           const ScoreParams& p, cudaStream_t st) {
   const ltk_config& c = h->cfg;
+  if (use_cc(&c)) {
+    CcParams cp{};
+    cp.q = p.q_raw;
+    cp.q_scale = p.q_scale;
+    cp.w = p.w;
+    cp.k_cache = p.k_raw;
+    cp.k_scale = p.k_scale;
+    cp.positions = p.positions;
+    cp.key_ids = p.key_ids;
+    cp.T = p.T;
+    cp.rows = p.rows;
+    cp.H = c.heads;
+    cp.d = c.dim;
+    cp.causal = p.causal;
+    cp.relu = c.relu;
+    cp.s_min = p.s_min;
+    cp.delta = p.delta;
+    cp.theta0 = p.theta0;
+    cp.cand = p.cand;
+    cp.cnt = p.cnt;
+    cp.ghist = p.ghist;
+    cp.cap = p.cap;
+    cp.nb = p.nb;
+    cp.k = p.k;
+    cp.refresh_interval = p.refresh_interval;
+    cp.b_full = p.b_full;
+    cp.s_last = p.s_last;
+    cp.status = p.status;
+    cp.dense = p.dense;
+    cp.ld = p.ld;
+    return launch_score_cc(mode, c.dtype == LTK_FP8_E4M3, cp, st);
+  }
   if (is_retrieval(&c))
     return launch_retrieval_tc(mode, qm, km, p, c.dim, c.relu, h->ghist, h->num_sms, st);
   return launch_score_tc(mode, c.dtype == LTK_FP8_E4M3, qm, km, p, st);
@@ -320,6 +369,35 @@ void plan_split(int T, long long S, int num_sms, int* b_full, int* s_last) {
   }
 }
 
+// Work units of the CUDA-core scorer: one query each; with fewer queries than
+// two per SM the key ranges are split (at least 8192 keys per range).
+void plan_split_cc(int T, long long S, int num_sms, int* b_full, int* s_last) {
+  *b_full = T;
+  *s_last = 1;
+  if (T <= 0 || T >= 2 * num_sms) return;
+  long long sl = (2ll * num_sms) / T;
+  const long long by_keys = S / 8192;
+  if (sl > by_keys) sl = by_keys;
+  if (sl > 64) sl = 64;
+  if (sl > 1) {
+    *b_full = 0;
+    *s_last = static_cast<int>(sl);
+  }
+}
+
+// Work plan for the handle's scorer; *queries_per_unit is how many queries one
+// unrolled unit covers (for the rows of split units).
+void plan_work(const ltk_handle* h, int T, long long S, int* b_full, int* s_last,
+               int* queries_per_unit) {
+  if (use_cc(&h->cfg)) {
+    plan_split_cc(T, S, h->num_sms, b_full, s_last);
+    *queries_per_unit = 1;
+  } else {
+    plan_split(T, S, h->num_sms, b_full, s_last);
+    *queries_per_unit = kTcQPB;
+  }
+}
+
 // Rows of q seen by TMA: [T * H, d].
 unsigned long long q_rows(const ltk_config& c, int T) {
   return static_cast<unsigned long long>(T) * c.heads;
@@ -358,11 +436,18 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   LTK_CUDA(launch_gather_keys(a.k_cache, a.k_scale, static_cast<int>(h->elem), c.dim, h->key_ids_pad,
                               n_pad, h->k_samp, h->k_scale_samp, st));
   CUtensorMap q_map, ks_map, k_map;
-  if (!make_tmap(&q_map, a.q, fp8, c.dim, q_rows(c, a.T), 256) ||
-      !make_tmap(&ks_map, h->k_samp, fp8, c.dim, n_pad, kTile) ||
-      !make_tmap(&k_map, a.k_cache, fp8, c.dim, static_cast<unsigned long long>(a.S), kTile))
+  std::memset(&q_map, 0, sizeof(q_map));
+  std::memset(&ks_map, 0, sizeof(ks_map));
+  std::memset(&k_map, 0, sizeof(k_map));
+  if (!use_cc(&c) &&
+      (!make_tmap(&q_map, a.q, fp8, c.dim, q_rows(c, a.T), 256) ||
+       !make_tmap(&ks_map, h->k_samp, fp8, c.dim, n_pad, kTile) ||
+       !make_tmap(&k_map, a.k_cache, fp8, c.dim, static_cast<unsigned long long>(a.S), kTile)))
     return LTK_ERR_CUDA;
+  int qpu = kTcQPB;
   ScoreParams sp{};
+  sp.q_raw = a.q;
+  sp.k_raw = h->k_samp;
   sp.w = a.w;
   sp.q_scale = a.q_scale;
   sp.k_scale = h->k_scale_samp;
@@ -374,7 +459,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   sp.dense = h->samp_scores;
   sp.ld = n_pad;
   sp.status = h->status;
-  plan_split(a.T, n_pad, h->num_sms, &sp.b_full, &sp.s_last);
+  plan_work(h, a.T, n_pad, &sp.b_full, &sp.s_last, &qpu);
   LTK_CUDA(launch_scorer(h, kModeDense, q_map, ks_map, sp, st));
   SampleStatsParams stp{h->samp_scores, n_pad, n_pad, a.T, a.k, c.n_bins, h->s_min, h->delta, h->theta0};
   LTK_CUDA(launch_sample_stats(stp, st));
@@ -382,6 +467,8 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
 
   // ---- Filter (Methodology step 2)
   ScoreParams fp{};
+  fp.q_raw = a.q;
+  fp.k_raw = a.k_cache;
   fp.w = a.w;
   fp.q_scale = a.q_scale;
   fp.k_scale = a.k_scale;
@@ -402,10 +489,10 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   fp.skip_key_loads = (c.debug_flags & 1) ? 1 : 0;
   fp.ghist = h->ghist;
   fp.status = h->status;
-  plan_split(a.T, a.S, h->num_sms, &fp.b_full, &fp.s_last);
+  plan_work(h, a.T, a.S, &fp.b_full, &fp.s_last, &qpu);
   if (!is_retrieval(&c) && fp.s_last > 1) {
     // split query blocks count and build histograms in global memory
-    const size_t t_first = static_cast<size_t>(fp.b_full) * kTcQPB;
+    const size_t t_first = static_cast<size_t>(fp.b_full) * qpu;
     const size_t n = static_cast<size_t>(a.T) - t_first;
     LTK_CUDA(cudaMemsetAsync(h->cnt + t_first, 0, n * sizeof(int), st));
     LTK_CUDA(cudaMemsetAsync(h->ghist + t_first * c.n_bins, 0, n * c.n_bins * sizeof(int), st));
@@ -680,10 +767,15 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   LTK_CUDA(cudaMemsetAsync(h->pairs, 0, sizeof(unsigned long long), st));
   LTK_CUDA(cudaMemsetAsync(h->ovf, 0, 2 * sizeof(int), st));
   CUtensorMap q_map, k_map;
-  if (!make_tmap(&q_map, q, fp8, c.dim, q_rows(c, T), 256) ||
-      !make_tmap(&k_map, k_cache, fp8, c.dim, static_cast<unsigned long long>(S), kTile))
+  std::memset(&q_map, 0, sizeof(q_map));
+  std::memset(&k_map, 0, sizeof(k_map));
+  if (!use_cc(&c) &&
+      (!make_tmap(&q_map, q, fp8, c.dim, q_rows(c, T), 256) ||
+       !make_tmap(&k_map, k_cache, fp8, c.dim, static_cast<unsigned long long>(S), kTile)))
     return LTK_ERR_CUDA;
   ScoreParams sp{};
+  sp.q_raw = q;
+  sp.k_raw = k_cache;
   sp.w = w;
   sp.q_scale = q_scale;
   sp.k_scale = k_scale;
@@ -695,7 +787,8 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   sp.dense = h->dense;
   sp.ld = S;
   sp.status = h->status;
-  plan_split(T, S, h->num_sms, &sp.b_full, &sp.s_last);
+  int qpu_d = kTcQPB;
+  plan_work(h, T, S, &sp.b_full, &sp.s_last, &qpu_d);
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
   LTK_CUDA(launch_scorer(h, kModeDense, q_map, k_map, sp, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[2], st));

@@ -354,6 +354,9 @@ struct ScoreParams {
   int b_full;
   int s_last;
   int* ghist;
+  // raw operand pointers (the CUDA-core scorer reads q and keys directly)
+  const void* q_raw;
+  const void* k_raw;
   // Dense output
   float* dense;            // [T, ld]
   long long ld;
@@ -460,6 +463,43 @@ struct RescueParams {
   int* out_idx;
   float* out_score;
 };
+
+// CUDA-core scorer with the fused affine bin map (k_score_cc.cu): any H <= 128,
+// d a multiple of 8 (16 for e4m3) up to 4096 (shared memory permitting).  Work units: query t, or one key
+// range of a split query (units [0, b_full) whole, then s_last ranges each).
+constexpr size_t kCcMaxSmem = 100 * 1024;
+struct CcParams {
+  const void* q;            // [T, H, d]
+  const float* q_scale;     // [T] (fp8)
+  const float* w;           // [T, H]
+  const void* k_cache;      // [rows, d]
+  const float* k_scale;     // [rows] (fp8)
+  const int* positions;     // [T] or null
+  const int* key_ids;       // dense mode over gathered rows, or null
+  int T;
+  long long rows;
+  int H;
+  int d;
+  int causal;
+  int relu;
+  const float* s_min;
+  const float* delta;
+  const int* theta0;
+  unsigned long long* cand;
+  int* cnt;
+  int* ghist;
+  int cap;
+  int nb;
+  int k;
+  int refresh_interval;
+  int b_full;
+  int s_last;
+  int* status;
+  float* dense;
+  long long ld;
+};
+size_t score_cc_smem_bytes(int H, int d, int nb);
+cudaError_t launch_score_cc(int mode, bool fp8, const CcParams& p, cudaStream_t stream);
 
 // LiteDSA packing (k_litedsa.cu): per group of G queries, the ascending union
 // of their selected indices and per-query membership masks.  Needs

@@ -33,7 +33,8 @@ class Config(ctypes.Structure):
                 ("cand_cap", ctypes.c_int), ("sample_size", ctypes.c_int),
                 ("seed", ctypes.c_ulonglong), ("refresh_interval", ctypes.c_int),
                 ("enable_decoupled", ctypes.c_int), ("rescue_rows", ctypes.c_int),
-                ("enable_host_io", ctypes.c_int), ("debug_flags", ctypes.c_int)]
+                ("enable_host_io", ctypes.c_int), ("engine", ctypes.c_int),
+                ("debug_flags", ctypes.c_int)]
 
 
 class Stats(ctypes.Structure):

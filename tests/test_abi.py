@@ -46,8 +46,8 @@ def test_workspace_sizing(ltk_lib):
 
 @pytest.mark.parametrize("field,value,status", [
     ("k", 0, 1), ("k", 8193, 1), ("max_S", 0, 1), ("max_S", 1 << 31, 1), ("n_bins", 100, 1),
-    ("n_bins", 16, 1), ("dtype", 7, 1), ("sample_size", 20000, 1), ("heads", 32, 6),
-    ("dim", 64, 6), ("relu", 0, 6), ("n_bins", 1024, 6), ("debug_flags", 2, 1),
+    ("n_bins", 16, 1), ("dtype", 7, 1), ("sample_size", 20000, 1), ("heads", 256, 6),
+    ("dim", 12, 6), ("dim", 8192, 6), ("n_bins", 8192, 6), ("debug_flags", 2, 1), ("engine", 3, 1),
 ])
 def test_invalid_configs_rejected_on_host(ltk_lib, field, value, status):
     cfg = _cfg(**{field: value})
@@ -73,3 +73,14 @@ def test_null_handle_calls_rejected(ltk_lib):
     assert ltk_lib.ltk_get_stats(None, None) == 1
     assert ltk_lib.ltk_set_timing(None, 1) == 1
     ltk_lib.ltk_destroy(None)
+
+
+@pytest.mark.parametrize("heads,dim,engine,status", [
+    (32, 64, 0, 0), (32, 64, 1, 6), (32, 64, 2, 0), (64, 128, 2, 0), (1, 768, 0, 0), (1, 768, 2, 0),
+    (200, 64, 0, 6), (64, 4104, 0, 6)])
+def test_engine_selection_on_host(ltk_lib, heads, dim, engine, status):
+    cfg = _cfg(heads=heads, dim=dim, engine=engine)
+    if heads == 1:
+        cfg.relu, cfg.causal, cfg.n_bins = 0, 0, 64
+    out = ctypes.c_ulonglong(0)
+    assert ltk_lib.ltk_workspace_bytes(ctypes.byref(cfg), ctypes.byref(out)) == status
