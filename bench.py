@@ -62,6 +62,8 @@ def parse_args():
                     help="queries per step of the reference (oracle) arm")
     ap.add_argument("--k", type=int, default=0,
                     help="retrieval workload: k (default 1000; the pages sweep 1024..8192)")
+    ap.add_argument("--engine", choices=["auto", "tensor", "cuda"], default="auto",
+                    help="scorer: tensor cores (default where the shape allows) or CUDA cores")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decoupled", action="store_true")
@@ -405,7 +407,8 @@ def run_decode(args):
     keys = datagen.keys_fp32(S, 128, 20260715 + rank)
     inp = datagen.make_indexer_inputs(T, S - T, S, dtype=args.dtype, seed=20260715 + rank, keys=keys)
     d = to_dev(inp, torch, dev)
-    op = IndexerTopK(max_T=T, max_S=S, k=2048, dtype=args.dtype)
+    op = IndexerTopK(max_T=T, max_S=S, k=2048, dtype=args.dtype,
+                     engine={"auto": 0, "tensor": 1, "cuda": 2}[args.engine])
     out = (torch.empty((T, 2048), dtype=torch.int32, device=dev),
            torch.empty((T, 2048), dtype=torch.float32, device=dev))
     first = op(d["q"], d["w"], d["k_cache"], d["positions"], k=2048, q_scale=d["q_scale"], k_scale=d["k_scale"])
@@ -431,7 +434,8 @@ def run_decode(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic (seeded hot-key/topic generator)",
             "config": {"workload": f"decode: T={T} queries at positions {S - T}..{S - 1}, S={S}, H=64, "
-                                   f"d=128, k=2048, previous-step sample; keys split over the GPU"},
+                                   f"d=128, k=2048, previous-step sample; keys split over the GPU",
+                       "engine": args.engine},
             "stages_ms": {"sample": st["ms_sample"], "filter": st["ms_filter"], "select": st["ms_select"]},
             "candidates_per_query": st["cand_written"] / T, "n_overflow": st["n_overflow"]}
     op.close()

@@ -370,15 +370,14 @@ void plan_split(int T, long long S, int num_sms, int* b_full, int* s_last) {
 }
 
 // Work units of the CUDA-core scorer: one query each; with fewer queries than
-// two per SM the key ranges are split (at least 8192 keys per range).
+// four per SM the key ranges are split (at least 4096 keys per range).
 void plan_split_cc(int T, long long S, int num_sms, int* b_full, int* s_last) {
   *b_full = T;
   *s_last = 1;
-  if (T <= 0 || T >= 2 * num_sms) return;
-  long long sl = (2ll * num_sms) / T;
-  const long long by_keys = S / 8192;
+  if (T <= 0 || T >= 4 * num_sms) return;
+  long long sl = (4ll * num_sms) / T;
+  const long long by_keys = S / 4096;
   if (sl > by_keys) sl = by_keys;
-  if (sl > 64) sl = 64;
   if (sl > 1) {
     *b_full = 0;
     *s_last = static_cast<int>(sl);
