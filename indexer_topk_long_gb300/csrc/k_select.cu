@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kSelThreads = 512;
 constexpr int kBndCap = 4096;        // boundary-bin entries held in shared memory
+constexpr int kRankSelect = 1024;    // boundary bins up to this size: select by rank counting
 
 // ---------------------------------------------------------------------------
 // Block helpers
@@ -191,6 +192,7 @@ __device__ void write_sorted(unsigned long long* buf, int kk, int k, int t, int*
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
   extern __shared__ unsigned long long sel_smem[];
   __shared__ int hist[kSelBins];
+  __shared__ int cur[kSelBins];
   __shared__ unsigned hist256[256];
   __shared__ long long sh[2];
   __shared__ float red[kSelThreads / 32];
@@ -276,13 +278,35 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   const int c_above = min(sh_int[1], kk);
   const int r = kk - c_above;
 
-  // pass C: bins above go straight to the output; the boundary bin is staged
+  // Bins above theta_f go straight to the output, already ordered by bin: each
+  // bin gets a slot range from a descending prefix sum of the histogram
+  // (highest bin first).  hist becomes the start offsets, cur the cursors.
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = kSelBins / 32;
+    const int top = kSelBins - lane * per;      // lane 0 owns the highest bins
+    int seg = 0;
+    for (int b = top - 1; b >= top - per; --b) seg += (b > theta_f) ? hist[b] : 0;
+    int incl = seg;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - seg;
+    for (int b = top - 1; b >= top - per; --b) {
+      const int h = (b > theta_f) ? hist[b] : 0;
+      hist[b] = run;
+      cur[b] = run;
+      run += h;
+    }
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const unsigned long long c = list[i];
     const float s = cand_score(c);
     const int b = bin_of(s, lo, delta, kSelBins);
     if (b > theta_f) {
-      const int slot = atomicAdd(&sh_int[2], 1);
+      const int slot = atomicAdd(&cur[b], 1);
       if (slot < kk) outbuf[slot] = ckey(s, cand_idx(c));
     } else if (b == theta_f) {
       const int slot = atomicAdd(&sh_int[3], 1);
@@ -292,32 +316,82 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
   __syncthreads();
   const int m_bnd = sh_int[3];
 
-  // exact top-r inside the boundary bin
+  // Order inside each bin above theta_f: a bin holds few entries, so one
+  // thread insertion-sorts its bins' ranges; if some bin is crowded (heavy
+  // ties), the whole output is sorted at the end instead.
+  bool crowded = false;
+  for (int b = threadIdx.x; b < kSelBins; b += blockDim.x) {
+    if (b <= theta_f) continue;
+    const int a0 = hist[b], a1 = min(cur[b], kk);
+    if (a1 - a0 > 32) {
+      crowded = true;
+      continue;
+    }
+    for (int i = a0 + 1; i < a1; ++i) {
+      const unsigned long long x = outbuf[i];
+      int j = i - 1;
+      while (j >= a0 && outbuf[j] < x) {
+        outbuf[j + 1] = outbuf[j];
+        --j;
+      }
+      outbuf[j + 1] = x;
+    }
+  }
+  const bool need_full_sort = __syncthreads_or(crowded ? 1 : 0) != 0;
+
+  // exact top-r inside the boundary bin, placed after the c_above entries
   if (r > 0) {
-    unsigned long long kth;
-    if (m_bnd <= kBndCap) {
-      kth = select_u64_smem(bnd, m_bnd, r, hist256, sh);
-      for (int i = threadIdx.x; i < m_bnd; i += blockDim.x)
-        if (bnd[i] >= kth) {
-          const int slot = atomicAdd(&sh_int[2], 1);
-          if (slot < kk) outbuf[slot] = bnd[i];
-        }
+    if (m_bnd <= kRankSelect) {
+      // the rank of each boundary key among the boundary keys is its output slot
+      for (int i = threadIdx.x; i < m_bnd; i += blockDim.x) {
+        const unsigned long long x = bnd[i];
+        int rank = 0;
+        for (int j = 0; j < m_bnd; ++j) rank += bnd[j] > x ? 1 : 0;
+        if (rank < r) outbuf[c_above + rank] = x;
+      }
     } else {
-      kth = select_u64_list(list, n, lo, delta, theta_f, r, hist256, sh);
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const unsigned long long c = list[i];
-        const float s = cand_score(c);
-        if (bin_of(s, lo, delta, kSelBins) != theta_f) continue;
-        const unsigned long long key = ckey(s, cand_idx(c));
-        if (key >= kth) {
-          const int slot = atomicAdd(&sh_int[2], 1);
-          if (slot < kk) outbuf[slot] = key;
+      if (threadIdx.x == 0) sh_int[2] = c_above;
+      __syncthreads();
+      unsigned long long kth;
+      if (m_bnd <= kBndCap) {
+        kth = select_u64_smem(bnd, m_bnd, r, hist256, sh);
+        for (int i = threadIdx.x; i < m_bnd; i += blockDim.x)
+          if (bnd[i] >= kth) {
+            const int slot = atomicAdd(&sh_int[2], 1);
+            if (slot < kk) outbuf[slot] = bnd[i];
+          }
+      } else {
+        kth = select_u64_list(list, n, lo, delta, theta_f, r, hist256, sh);
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+          const unsigned long long c = list[i];
+          const float s = cand_score(c);
+          if (bin_of(s, lo, delta, kSelBins) != theta_f) continue;
+          const unsigned long long key = ckey(s, cand_idx(c));
+          if (key >= kth) {
+            const int slot = atomicAdd(&sh_int[2], 1);
+            if (slot < kk) outbuf[slot] = key;
+          }
         }
       }
     }
   }
   __syncthreads();
-  write_sorted(outbuf, min(sh_int[2], kk), p.k, t, p.out_idx, p.out_score);
+  // a large boundary bin was selected unordered: sort the whole output
+  if (need_full_sort || (r > 0 && m_bnd > kRankSelect)) {
+    write_sorted(outbuf, kk, p.k, t, p.out_idx, p.out_score);
+  } else {
+    int* oi = p.out_idx + static_cast<size_t>(t) * p.k;
+    float* os = p.out_score + static_cast<size_t>(t) * p.k;
+    for (int i = threadIdx.x; i < p.k; i += blockDim.x) {
+      if (i < kk) {
+        oi[i] = ckey_idx(outbuf[i]);
+        os[i] = ckey_score(outbuf[i]);
+      } else {
+        oi[i] = -1;
+        os[i] = -INFINITY;
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
