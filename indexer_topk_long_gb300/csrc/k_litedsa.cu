@@ -132,13 +132,9 @@ cudaError_t launch_litedsa_pack(const int* topk, int T, int k, int G, int* union
   if (n_groups == 0) return cudaSuccess;
   const int W = (G * k + 31) / 32;
   const size_t smem = litedsa_smem_bytes(G, k);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(litedsa_pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kLitedsaMaxSmem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(litedsa_pack_kernel), kSlotLitedsa,
+                                    kLitedsaMaxSmem);
+  if (e != cudaSuccess) return e;
   litedsa_pack_kernel<<<n_groups, kLdThreads, smem, stream>>>(topk, T, k, G, W, union_idx, union_len,
                                                               masks);
   count_launches(1);

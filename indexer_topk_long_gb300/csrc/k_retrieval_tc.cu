@@ -369,14 +369,10 @@ cudaError_t launch_r(const CUtensorMap& qm, const CUtensorMap& cm, const ScorePa
   const int per = (total_tiles + n_split - 1) / n_split;
   n_split = (total_tiles + per - 1) / per;
   const size_t smem = r_smem_bytes(MODE == kModeFilter ? p.nb : 0);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(retrieval_tc_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(r_smem_bytes(MODE == kModeFilter ? kRetrievalMaxBins : 0)));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(retrieval_tc_kernel<MODE>),
+                                    kSlotRetrieval + MODE,
+                                    r_smem_bytes(MODE == kModeFilter ? kRetrievalMaxBins : 0));
+  if (e != cudaSuccess) return e;
   retrieval_tc_kernel<MODE><<<t_blocks * n_split, kRThreads, smem, stream>>>(
       qm, cm, p, dim / 64, t_blocks, per, relu, ghist);
   count_launches(1);

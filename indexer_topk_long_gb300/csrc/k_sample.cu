@@ -345,14 +345,9 @@ cudaError_t launch_prepare_sample(const int* ids, int n, long long S, int n_pad,
   int P = 1;
   while (P < n) P <<= 1;
   const size_t smem = static_cast<size_t>(P) * sizeof(int);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prepare_sample_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kMaxSample * sizeof(int)));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prepare_sample_kernel), kSlotPrepare,
+                                    kMaxSample * sizeof(int));
+  if (e != cudaSuccess) return e;
   prepare_sample_kernel<<<1, kPrepThreads, smem, stream>>>(ids, n, S, n_pad, key_ids_pad);
   count_launches(1);
   return cudaGetLastError();
@@ -375,14 +370,9 @@ cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int el
 cudaError_t launch_sample_stats(const SampleStatsParams& p, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
   const size_t smem = static_cast<size_t>(p.n) * sizeof(uint32_t);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(sample_stats_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kMaxSample * sizeof(uint32_t)));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(sample_stats_kernel), kSlotStats,
+                                    kMaxSample * sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
   sample_stats_kernel<<<p.T, kStatsThreads, smem, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();

@@ -299,14 +299,9 @@ cudaError_t launch_cc(const CcParams& p, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
   const int grid = p.b_full + (p.T - p.b_full) * (p.s_last > 1 ? p.s_last : 1);
   const size_t smem = score_cc_smem_bytes(p.H, p.d, MODE == kModeFilter ? p.nb : 0);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(score_cc_kernel<MODE, FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kCcMaxSmem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(score_cc_kernel<MODE, FP8>),
+                                    kSlotScoreCc + MODE * 2 + (FP8 ? 1 : 0), kCcMaxSmem);
+  if (e != cudaSuccess) return e;
   score_cc_kernel<MODE, FP8><<<grid, kCcThreads, smem, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();

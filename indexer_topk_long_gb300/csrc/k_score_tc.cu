@@ -531,14 +531,10 @@ cudaError_t launch_one(const CUtensorMap& qm, const CUtensorMap& km, const Score
   if (t_blocks == 0) return cudaSuccess;
   const int grid = p.b_full + (t_blocks - p.b_full) * (p.s_last > 1 ? p.s_last : 1);
   const size_t smem = smem_bytes<FP8>(MODE == kModeFilter ? p.nb : 0);
-  static size_t configured = 0;
-  if (configured < smem) {
-    cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<MODE, FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes<FP8>(Shape<FP8>::kMaxBins)));
-    if (e != cudaSuccess) return e;
-    configured = smem_bytes<FP8>(Shape<FP8>::kMaxBins);
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(score_tc_kernel<MODE, FP8>),
+                                    kSlotScoreTc + MODE * 2 + (FP8 ? 1 : 0),
+                                    smem_bytes<FP8>(Shape<FP8>::kMaxBins));
+  if (e != cudaSuccess) return e;
   score_tc_kernel<MODE, FP8><<<grid, kThreads, smem, stream>>>(qm, km, p);
   count_launches(1);
   return cudaGetLastError();

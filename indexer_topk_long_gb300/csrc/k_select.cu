@@ -685,14 +685,9 @@ size_t outbuf_bytes(int k) {
 cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
   const size_t smem = outbuf_bytes(p.k) + kBndCap * sizeof(unsigned long long);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(outbuf_bytes(kMaxK) +
-                                                          kBndCap * sizeof(unsigned long long)));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), kSlotSelect,
+                                    outbuf_bytes(kMaxK) + kBndCap * sizeof(unsigned long long));
+  if (e != cudaSuccess) return e;
   select_kernel<<<p.T, kSelThreads, smem, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();
@@ -701,13 +696,9 @@ cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
 cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
   const size_t smem = outbuf_bytes(p.k);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(row_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(outbuf_bytes(kMaxK)));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(row_topk_kernel), kSlotRowTopk,
+                                    outbuf_bytes(kMaxK));
+  if (e != cudaSuccess) return e;
   row_topk_kernel<<<p.T, kSelThreads, smem, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();
@@ -717,14 +708,9 @@ cudaError_t launch_rescue(const RescueParams& p, int rescue_rows, cudaStream_t s
   if (p.T <= 0 || rescue_rows <= 0) return cudaSuccess;
   const size_t qbytes = static_cast<size_t>(p.heads) * p.dim * sizeof(float);
   const size_t smem = qbytes > outbuf_bytes(p.k) ? qbytes : outbuf_bytes(p.k);
-  static bool configured = false;
-  if (!configured) {
-    const size_t mx = kCcMaxSmem > outbuf_bytes(kMaxK) ? kCcMaxSmem : outbuf_bytes(kMaxK);
-    cudaError_t e = cudaFuncSetAttribute(rescue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(mx));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const size_t mx = kCcMaxSmem > outbuf_bytes(kMaxK) ? kCcMaxSmem : outbuf_bytes(kMaxK);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(rescue_kernel), kSlotRescue, mx);
+  if (e != cudaSuccess) return e;
   rescue_kernel<<<rescue_rows, kRescueThreads, smem, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();

@@ -73,6 +73,23 @@ namespace {
 std::atomic<long long> g_launches{0};
 }
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+constexpr int kMaxDevices = 256;
+std::atomic<unsigned int> g_smem_done[kMaxDevices] = {};   // bit per slot
+}
+
+cudaError_t ensure_smem_limit(const void* func, int slot, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const unsigned int bit = 1u << slot;
+  if (g_smem_done[dev].load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) g_smem_done[dev].fetch_or(bit, std::memory_order_release);
+  return e;
+}
 long long launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
 }  // namespace ltk
 

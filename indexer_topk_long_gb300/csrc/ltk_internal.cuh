@@ -321,6 +321,23 @@ __host__ __device__ constexpr uint32_t make_idesc(bool fp8, int M, int N) {
 // ---------------------------------------------------------------------------
 // Kernel parameter blocks and launch functions (defined in the kernel files)
 // ---------------------------------------------------------------------------
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device (the attribute is per device; set once per device and kernel).
+// `slot` identifies the kernel (a small distinct integer per call site).
+cudaError_t ensure_smem_limit(const void* func, int slot, size_t bytes);
+enum SmemSlot {
+  kSlotScoreTc = 0,          // 4 instantiations: + mode * 2 + fp8
+  kSlotRetrieval = 4,        // 2 instantiations: + mode
+  kSlotScoreCc = 6,          // 4 instantiations: + mode * 2 + fp8
+  kSlotPrepare = 10,
+  kSlotStats = 11,
+  kSlotSelect = 12,
+  kSlotRowTopk = 13,
+  kSlotRescue = 14,
+  kSlotLitedsa = 15,
+  kSlotCount = 16
+};
+
 // Process-wide count of kernels launched by this library (ltk_api.cu).
 void count_launches(int n);
 long long launches_so_far();
