@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
           const int col0 = ch * 128 + cc * 32;
           float v[32];
           tmem_ld32(tmem + lane_base + buf * kRN + col0, v);
-          tmem_wait_ld();
+          tmem_wait_ld_tied(v);
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             const int q = col0 + jj;

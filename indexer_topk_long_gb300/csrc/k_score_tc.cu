@@ -87,13 +87,14 @@ constexpr size_t smem_bytes(int nb) {
 // (lanes 0-15 and 16-31 of the quarter), so thread t (c = t % 4) holds 16
 // heads {8r + 2c + i} of the 4 keys t/4 + {0, 8, 16, 24}.
 //
-// Partial weighted head sums of one query for 2 keys: va holds a 16x256b x8
-// load (64 columns of 16 lanes), so thread t (c = t % 4) has heads
-// h = 8r + 2c + {0, 1} of keys t/4 and t/4 + 8; w2[r] packs the weights of
-// that head pair.  Each packed FMA covers one head pair of one key.  The even
-// head's ReLU is max(x, 0) (ALU pipe); the odd head uses x + |x| = 2 max(x, 0)
-// (FMA pipe) and its accumulator half is halved at the end, which is exact, so
-// the sums equal sum_h w[h] * max(0, x[h]) accumulated in this order.
+// Partial weighted head sums of one query for 2 keys over 16 heads: v holds a
+// 16x256b x4 load (32 columns of 16 lanes), so thread t (c = t % 4) has heads
+// h = 8(roff + r) + 2c + {0, 1} of keys t/4 and t/4 + 8 for r = 0..3; w2 packs
+// the weights of each head pair.  Each packed FMA covers one head pair of one
+// key.  The even head's ReLU is max(x, 0) (ALU pipe); the odd head uses
+// x + |x| = 2 max(x, 0) (FMA pipe) and its accumulator half is halved at the
+// end (fold_pair), which is exact, so the sums equal sum_h w[h] * max(0, x[h])
+// accumulated in head order.
 __device__ __forceinline__ float relu_twice(float x) { return __fadd_rn(x, fabsf(x)); }
 
 __device__ __forceinline__ float fold_pair(unsigned long long acc) {
@@ -102,14 +103,14 @@ __device__ __forceinline__ float fold_pair(unsigned long long acc) {
   return __fmaf_rn(hi, 0.5f, lo);
 }
 
-__device__ __forceinline__ float2 head_partials(const float* va, const unsigned long long (&w2)[8]) {
-  unsigned long long a0 = 0ull, a1 = 0ull;   // (+0.f, +0.f)
+__device__ __forceinline__ void head_partials(unsigned long long& a0, unsigned long long& a1,
+                                              const float (&v)[16],
+                                              const unsigned long long (&w2)[8], int roff) {
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    ffma2_acc(a0, fmaxf(va[4 * r + 0], 0.f), relu_twice(va[4 * r + 1]), w2[r]);
-    ffma2_acc(a1, fmaxf(va[4 * r + 2], 0.f), relu_twice(va[4 * r + 3]), w2[r]);
+  for (int r = 0; r < 4; ++r) {
+    ffma2_acc(a0, fmaxf(v[4 * r + 0], 0.f), relu_twice(v[4 * r + 1]), w2[roff + r]);
+    ffma2_acc(a1, fmaxf(v[4 * r + 2], 0.f), relu_twice(v[4 * r + 3]), w2[roff + r]);
   }
-  return make_float2(fold_pair(a0), fold_pair(a1));
 }
 
 // Reduce-scatter over the quad of threads that hold the same 4 keys
@@ -465,18 +466,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // read the query's 64 columns, then hand the TMEM half back at once
+          // read the query's 64 columns of the warp's 32 lanes in four 16-lane x
+          // 32-column pieces, each load in flight while the previous piece is
+          // summed; the TMEM half goes back as soon as the last piece has landed
           const uint32_t ta = tq0 + j * kN;
-          float va[32], vb[32];
-          tmem_ld16x256b_x8(ta, va);
-          tmem_ld16x256b_x8(ta + (16u << 16), vb);
-          tmem_wait_ld();
+          float c0[16], c1[16], c2[16], c3[16];
+          unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;   // (+0.f, +0.f)
+          tmem_ld16x256b_x4(ta, c0);
+          tmem_wait_ld_tied(c0);
+          tmem_ld16x256b_x4(ta + 32u, c1);
+          head_partials(a0, a1, c0, wr[j], 0);
+          tmem_wait_ld_tied(c1);
+          tmem_ld16x256b_x4(ta + (16u << 16), c2);
+          head_partials(a0, a1, c1, wr[j], 4);
+          tmem_wait_ld_tied(c2);
+          tmem_ld16x256b_x4(ta + (16u << 16) + 32u, c3);
+          head_partials(b0, b1, c2, wr[j], 0);
+          tmem_wait_ld_tied(c3);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty0 + 8 * j);
-          const float2 pa = head_partials(va, wr[j]);
-          const float2 pb = head_partials(vb, wr[j]);
-          float I = quad_reduce(pa.x, pa.y, pb.x, pb.y, c);
+          head_partials(b0, b1, c3, wr[j], 4);
+          float I = quad_reduce(fold_pair(a0), fold_pair(a1), fold_pair(b0), fold_pair(b1), c);
           const int ql = j * 4 + qh;            // query within the CTA
           if constexpr (FP8) I = __fmul_rn(I, kscale);
           if constexpr (MODE == kModeDense) {
