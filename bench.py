@@ -62,6 +62,8 @@ def parse_args():
                     help="queries per step of the reference (oracle) arm")
     ap.add_argument("--k", type=int, default=0,
                     help="retrieval workload: k (default 1000; the pages sweep 1024..8192)")
+    ap.add_argument("--corpus", type=int, default=0,
+                    help="retrieval workload: corpus rows (default 8388608; smaller for profiling)")
     ap.add_argument("--engine", choices=["auto", "tensor", "cuda"], default="auto",
                     help="scorer: tensor cores (default where the shape allows) or CUDA cores")
     ap.add_argument("--no-e2e", action="store_true")
@@ -288,6 +290,8 @@ def run_retrieval(args):
     if args.k:
         R["k"] = args.k
         R["sample"] = min(3 * args.k, 16384)
+    if args.corpus:
+        R["N"] = args.corpus
     T = args.queries or R["T"]
     q, c = datagen.retrieval_inputs_torch(R["N"], T, R["d"], seed=20260715 + rank, device=dev)
     w = torch.ones((T, 1), dtype=torch.float32, device=dev)
@@ -325,7 +329,9 @@ def run_retrieval(args):
     flop = 2 * R["d"] * pairs
     achieved = flop / (st["ms_filter"] * 1e-3) / 1e12
     line = {
-        "metric": RETRIEVAL_METRIC, "value": whole_job_value(pairs, args.steps, world, elapsed),
+        "metric": (RETRIEVAL_METRIC if R["N"] == RETRIEVAL["N"]
+                   else RETRIEVAL_METRIC.replace("8.4M", str(R["N"]))),
+        "value": whole_job_value(pairs, args.steps, world, elapsed),
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (clustered Gaussian corpus; MSMARCO unavailable)",

@@ -16,7 +16,10 @@
 //     3-deep ring of (16 KB corpus chunk + 32 KB query chunk).
 //   * TMEM holds two 256-column accumulators: the epilogue drains one corpus
 //     tile while the tensor core computes the next.
-//   * Epilogue (8 warps): each thread owns one corpus row and 128 query columns.
+//   * Epilogue (16 warps, four per scheduler, so that the latency of one warp's
+//     global append is covered by the others): each thread owns one corpus row
+//     and 64 query columns, read from TMEM 16 columns at a time, each load in
+//     flight while the previous 16 columns are gated.
 //     The gate "bin >= theta" is evaluated as one compare against a per-query
 //     score threshold tau = the smallest float whose bin is >= theta (found by
 //     binary search over float order, so the two tests agree exactly).
@@ -38,9 +41,9 @@
 namespace ltk {
 namespace {
 
-constexpr int kRThreads = 384;
+constexpr int kRThreads = 640;
 constexpr int kREpiWarp0 = 4;
-constexpr int kREpiWarps = 8;
+constexpr int kREpiWarps = 16;
 constexpr int kRRefreshWarp = 2;
 constexpr int kRN = 256;                 // queries per CTA (MMA N)
 constexpr int kRStages = 3;
@@ -50,10 +53,10 @@ constexpr int kRStage = kRAChunk + kRBChunk;
 constexpr uint32_t kRTmemCols = 512;
 
 struct QState {
-  float tau;      // gate threshold in score space
   float s_min;
   float delta;
   int theta;
+  int pad;
 };
 
 struct __align__(8) RCtrl {
@@ -73,7 +76,7 @@ struct __align__(8) RCtrl {
 __host__ __device__ constexpr int r_hist_stride(int nb) { return nb + 1; }
 
 constexpr size_t r_smem_bytes(int nb) {
-  return 1024 + static_cast<size_t>(kRStages) * kRStage + kRN * sizeof(QState) + kRN * sizeof(float) +
+  return 1024 + static_cast<size_t>(kRStages) * kRStage + kRN * sizeof(QState) + kRN * sizeof(float2) +
          sizeof(RCtrl) + static_cast<size_t>(kRN) * (nb > 0 ? r_hist_stride(nb) : 0) * sizeof(int);
 }
 
@@ -93,11 +96,30 @@ __device__ float gate_tau(int theta, float s_min, float delta, int nb) {
   return unord_f32(hi);
 }
 
-template <int MODE>
+// Append the passing rows of one query (whole warp; m = the warp's pass mask,
+// nonzero): one global atomic reserves the slots, every passing lane writes
+// its (score, row) record and counts it in the query's shared histogram.  Kept
+// out of line so that the epilogue's per-query loop stays small in the
+// instruction cache; it runs only for (query, 32-row) blocks with a pass.
+__device__ __noinline__ void append_passes(const ScoreParams& p, int gq, unsigned m, bool pass,
+                                           float I, int key, int* hrow, float s_min, float delta) {
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(&p.cnt[gq], __popc(m));
+  base = __shfl_sync(0xFFFFFFFFu, base, leader);
+  if (pass) {
+    const int slot = base + __popc(m & ((1u << lane) - 1u));
+    if (slot < p.cap) p.cand[static_cast<size_t>(gq) * p.cap + slot] = cand_pack(I, key);
+    atomicAdd(&hrow[bin_of(I, s_min, delta, p.nb)], 1);
+  }
+}
+
+template <int MODE, bool RELU>
 __global__ void __launch_bounds__(kRThreads, 1)
     retrieval_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                         const __grid_constant__ CUtensorMap c_map, const ScoreParams p,
-                        int n_chunks, int t_blocks, int tiles_per_split, int relu,
+                        int n_chunks, int t_blocks, int tiles_per_split,
                         int* ghist) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -105,8 +127,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
   uint8_t* smem = smem_raw + pad;
   const uint32_t s_stage = raw + pad;
   QState* qs = reinterpret_cast<QState*>(smem + kRStages * kRStage);
-  float* wq = reinterpret_cast<float*>(qs + kRN);
-  RCtrl* ctrl = reinterpret_cast<RCtrl*>(wq + kRN);
+  float2* tw = reinterpret_cast<float2*>(qs + kRN);   // per query {gate threshold tau, weight}
+  RCtrl* ctrl = reinterpret_cast<RCtrl*>(tw + kRN);
   int* hist = reinterpret_cast<int*>(ctrl + 1);
   const int hstride = r_hist_stride(p.nb);
   volatile int* abort_flag = &ctrl->abort_flag;
@@ -122,16 +144,18 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   for (int q = tid; q < kRN; q += kRThreads) {
     const bool ok = q < nq;
-    wq[q] = ok ? p.w[t0 + q] : 0.f;
+    float tau = INFINITY;
     if constexpr (MODE == kModeFilter) {
       QState st;
       st.s_min = ok ? p.s_min[t0 + q] : 0.f;
       st.delta = ok ? p.delta[t0 + q] : 0.f;
       const int th = ok ? p.theta0[t0 + q] : 0;
       st.theta = th;
-      st.tau = gate_tau(th, st.s_min, st.delta, p.nb);
+      st.pad = 0;
+      if (ok) tau = gate_tau(th, st.s_min, st.delta, p.nb);
       qs[q] = st;
     }
+    tw[q] = make_float2(tau, ok ? p.w[t0 + q] : 0.f);
   }
   if constexpr (MODE == kModeFilter) {
     for (int i = tid; i < kRN * hstride; i += kRThreads) hist[i] = 0;
@@ -266,7 +290,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                   }
                   if (found > cur) {
                     const QState st = qs[q];
-                    *reinterpret_cast<volatile float*>(&qs[q].tau) = gate_tau(found, st.s_min, st.delta, p.nb);
+                    *reinterpret_cast<volatile float*>(&tw[q].x) = gate_tau(found, st.s_min, st.delta, p.nb);
                     *reinterpret_cast<volatile int*>(&qs[q].theta) = found;
                   }
                 }
@@ -289,7 +313,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     } else if (warp >= kREpiWarp0) {
       // ---------------- epilogue ----------------
       const int lq = warp & 3;
-      const int ch = (warp - kREpiWarp0) >> 2;      // which 128 of the 256 query columns
+      const int ch = (warp - kREpiWarp0) >> 2;      // which 64 of the 256 query columns
       const int row = lq * 32 + lane;
       const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
       const int rows_i = static_cast<int>(p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF);
@@ -303,44 +327,52 @@ __global__ void __launch_bounds__(kRThreads, 1)
         const bool key_ok = key < rows_i;
         int kid = key;
         if (MODE == kModeDense && p.key_ids != nullptr) kid = key_ok ? p.key_ids[key] : INT_MAX;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          const int col0 = ch * 128 + cc * 32;
-          float v[32];
-          tmem_ld32(tmem + lane_base + buf * kRN + col0, v);
-          tmem_wait_ld_tied(v);
+        // gate (or store) 16 query columns of this thread's corpus row
+        auto columns = [&](const float (&v)[16], const int col0) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
+          for (int jj = 0; jj < 16; ++jj) {
             const int q = col0 + jj;
-            float I = relu ? fmaxf(v[jj], 0.f) : v[jj];
-            I = __fmul_rn(I, wq[q]);
             if constexpr (MODE == kModeDense) {
+              const float I = __fmul_rn(RELU ? fmaxf(v[jj], 0.f) : v[jj], tw[q].y);
               if (q < nq && key_ok)
                 p.dense[static_cast<size_t>(t0 + q) * p.ld + key] = (kid != INT_MAX) ? I : -INFINITY;
             } else {
-              const float tau = *reinterpret_cast<volatile float*>(&qs[q].tau);
-              const bool pass = key_ok && q < nq && I >= tau;
+              // {tau, w} in one load; tau is rewritten by the refresh warp
+              const unsigned long long g = *reinterpret_cast<volatile unsigned long long*>(&tw[q]);
+              const float I = __fmul_rn(RELU ? fmaxf(v[jj], 0.f) : v[jj],
+                                        __uint_as_float(static_cast<uint32_t>(g >> 32)));
+              const bool pass = key_ok && q < nq && I >= __uint_as_float(static_cast<uint32_t>(g));
               const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
-              if (m != 0) {
-                const int leader = __ffs(m) - 1;
-                int base = 0;
-                if (lane == leader) base = atomicAdd(&p.cnt[t0 + q], __popc(m));
-                base = __shfl_sync(0xFFFFFFFFu, base, leader);
-                if (pass) {
-                  const int slot = base + __popc(m & ((1u << lane) - 1u));
-                  if (slot < p.cap) p.cand[static_cast<size_t>(t0 + q) * p.cap + slot] = cand_pack(I, key);
-                  const QState st = qs[q];
-                  atomicAdd(&hist[q * hstride + bin_of(I, st.s_min, st.delta, p.nb)], 1);
-                }
+              if (m != 0u) {
+                const QState st = qs[q];
+                append_passes(p, t0 + q, m, pass, I, key, hist + q * hstride, st.s_min, st.delta);
               }
             }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&ctrl->acc_empty[buf]));
-          atomicAdd(&ctrl->tiles_done, 1);
+        };
+        const uint32_t tbase = tmem + lane_base + buf * kRN + ch * 64;
+        float va[16], vb[16];
+        tmem_ld32x16(tbase, va);
+        tmem_wait_ld_tied(va);
+#pragma unroll 1
+        for (int c2 = 0; c2 < 64; c2 += 32) {
+          // piece c2 + 16 loads while piece c2 is gated, and so on
+          tmem_ld32x16(tbase + c2 + 16u, vb);
+          columns(va, ch * 64 + c2);
+          tmem_wait_ld_tied(vb);
+          if (c2 == 0) {
+            tmem_ld32x16(tbase + 32u, va);
+          } else {
+            // every column of this tile is in registers: hand the accumulator back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(smem_u32(&ctrl->acc_empty[buf]));
+              atomicAdd(&ctrl->tiles_done, 1);
+            }
+          }
+          columns(vb, ch * 64 + c2 + 16);
+          if (c2 == 0) tmem_wait_ld_tied(va);
         }
       }
     }
@@ -355,9 +387,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
 }
 
-template <int MODE>
+template <int MODE, bool RELU>
 cudaError_t launch_r(const CUtensorMap& qm, const CUtensorMap& cm, const ScoreParams& p, int dim,
-                     int relu, int* ghist, int num_sms, cudaStream_t stream) {
+                     int* ghist, int num_sms, cudaStream_t stream) {
   const int t_blocks = (p.T + kRN - 1) / kRN;
   if (t_blocks == 0) return cudaSuccess;
   const int total_tiles = static_cast<int>((p.rows + kTile - 1) / kTile);
@@ -369,12 +401,12 @@ cudaError_t launch_r(const CUtensorMap& qm, const CUtensorMap& cm, const ScorePa
   const int per = (total_tiles + n_split - 1) / n_split;
   n_split = (total_tiles + per - 1) / per;
   const size_t smem = r_smem_bytes(MODE == kModeFilter ? p.nb : 0);
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(retrieval_tc_kernel<MODE>),
-                                    kSlotRetrieval + MODE,
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(retrieval_tc_kernel<MODE, RELU>),
+                                    kSlotRetrieval + MODE * 2 + (RELU ? 1 : 0),
                                     r_smem_bytes(MODE == kModeFilter ? kRetrievalMaxBins : 0));
   if (e != cudaSuccess) return e;
-  retrieval_tc_kernel<MODE><<<t_blocks * n_split, kRThreads, smem, stream>>>(
-      qm, cm, p, dim / 64, t_blocks, per, relu, ghist);
+  retrieval_tc_kernel<MODE, RELU><<<t_blocks * n_split, kRThreads, smem, stream>>>(
+      qm, cm, p, dim / 64, t_blocks, per, ghist);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -387,8 +419,10 @@ cudaError_t launch_retrieval_tc(int mode, const CUtensorMap& q_map, const CUtens
                                 const ScoreParams& p, int dim, int relu, int* ghist,
                                 int num_sms, cudaStream_t stream) {
   if (mode == kModeDense)
-    return launch_r<kModeDense>(q_map, c_map, p, dim, relu, ghist, num_sms, stream);
-  return launch_r<kModeFilter>(q_map, c_map, p, dim, relu, ghist, num_sms, stream);
+    return relu ? launch_r<kModeDense, true>(q_map, c_map, p, dim, ghist, num_sms, stream)
+                : launch_r<kModeDense, false>(q_map, c_map, p, dim, ghist, num_sms, stream);
+  return relu ? launch_r<kModeFilter, true>(q_map, c_map, p, dim, ghist, num_sms, stream)
+              : launch_r<kModeFilter, false>(q_map, c_map, p, dim, ghist, num_sms, stream);
 }
 
 }  // namespace ltk

@@ -231,6 +231,18 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane (shape 32x32b, 16
+// repetitions).  Undefined until tmem_wait_ld_tied on the same array.
+__device__ __forceinline__ void tmem_ld32x16(uint32_t taddr, float (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
+        "=f"(v[14]), "=f"(v[15])
+      : "r"(taddr));
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane (shape 32x32b, 32
 // repetitions).  Undefined until tmem_wait_ld_tied on the same array.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -338,15 +350,15 @@ __host__ __device__ constexpr uint32_t make_idesc(bool fp8, int M, int N) {
 cudaError_t ensure_smem_limit(const void* func, int slot, size_t bytes);
 enum SmemSlot {
   kSlotScoreTc = 0,          // 4 instantiations: + mode * 2 + fp8
-  kSlotRetrieval = 4,        // 2 instantiations: + mode
-  kSlotScoreCc = 6,          // 4 instantiations: + mode * 2 + fp8
-  kSlotPrepare = 10,
-  kSlotStats = 11,
-  kSlotSelect = 12,
-  kSlotRowTopk = 13,
-  kSlotRescue = 14,
-  kSlotLitedsa = 15,
-  kSlotCount = 16
+  kSlotRetrieval = 4,        // 4 instantiations: + mode * 2 + relu
+  kSlotScoreCc = 8,          // 4 instantiations: + mode * 2 + fp8
+  kSlotPrepare = 12,
+  kSlotStats = 13,
+  kSlotSelect = 14,
+  kSlotRowTopk = 15,
+  kSlotRescue = 16,
+  kSlotLitedsa = 17,
+  kSlotCount = 18
 };
 
 // Process-wide count of kernels launched by this library (ltk_api.cu).
