@@ -102,24 +102,28 @@ def measured_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+SCORE_TC_SOURCES = ["indexer_topk_long_gb300/csrc/k_score_tc.cu", "indexer_topk_long_gb300/csrc/ltk_internal.cuh"]
+RETRIEVAL_SOURCES = ["indexer_topk_long_gb300/csrc/k_retrieval_tc.cu", "indexer_topk_long_gb300/csrc/ltk_internal.cuh"]
+
+
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in ["indexer_topk_long_gb300/csrc/k_score_tc.cu", "indexer_topk_long_gb300/csrc/ltk_internal.cuh"]:
+    for rel in sources or SCORE_TC_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, dtype: str):
-    """DRAM bytes per filter-kernel launch from the committed ncu summary, if it
-    was captured on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"score_filter_{workload}_{dtype}.md")
+def recorded_traffic(profile: str, sources=None):
+    """DRAM bytes per filter-kernel launch from the committed ncu summary
+    profiles/<profile>.md, if it was captured on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{profile}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     hsh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    if not m or not hsh or hsh.group(1) != kernel_source_hash():
+    if not m or not hsh or hsh.group(1) != kernel_source_hash(sources):
         return None
     return float(m.group(1))
 
@@ -337,9 +341,12 @@ def run_retrieval(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (clustered Gaussian corpus; MSMARCO unavailable)",
         "config": {"workload": f"vector retrieval: {T} queries x {R['N']} corpus rows, d={R['d']}, "
                                f"k={R['k']}, H=1, no ReLU, no mask, {R['sample']} random sample rows",
-                   "l2": "inputs larger than L2 (corpus 12.9 GB)"},
+                   "l2": f"inputs larger than L2 (corpus {R['N'] * R['d'] * 2 / 1e9:.1f} GB)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "retrieval_tc_kernel<filter>",
+                     "frac": achieved / peak,
+                     "traffic": (recorded_traffic(f"retrieval_filter_8m_k{R['k']}", RETRIEVAL_SOURCES)
+                                 if R["N"] == RETRIEVAL["N"] and T == RETRIEVAL["T"] else None),
+                     "kernel": "retrieval_tc_kernel<filter>",
                      "peak_source": f"{kind} bf16 sustained", "algorithmic_flop_per_launch": flop},
         "gpu_launches": st["launches"] - launches0, "clocks": clock_info,
         "stages_ms": {"sample": st["ms_sample"], "filter": st["ms_filter"], "select": st["ms_select"],
@@ -535,7 +542,7 @@ def main():
     bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     peak = bf16_peak * (FP8_OVER_BF16 if args.dtype == "fp8" else 1.0)
     achieved = FLOP_PER_PAIR * pairs_step / (st["ms_filter"] * 1e-3) / 1e12
-    traffic = recorded_traffic(args.workload, args.dtype)
+    traffic = recorded_traffic(f"score_filter_{args.workload}_{args.dtype}")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "kernel": "score_tc_kernel<filter> (fused score + bin + gate + write-back)",

@@ -466,6 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // the threshold is read before the scores (any value read is a valid
+          // lower bound), so the load's latency overlaps the TMEM loads
+          int th_pre = 0;
+          if constexpr (MODE == kModeFilter) th_pre = *reinterpret_cast<volatile int*>(&ctrl->theta[j * 4 + qh]);
           // read the query's 64 columns of the warp's 32 lanes in four 16-lane x
           // 32-column pieces, each load in flight while the previous piece is
           // summed; the TMEM half goes back as soon as the last piece has landed
@@ -498,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             const int b = bin_of(I, qs_min[j], qdelta[j], p.nb);
-            const int th = *reinterpret_cast<volatile int*>(&ctrl->theta[ql]);
+            const int th = th_pre;
             const bool pass = key <= last_key[j] && b >= th;
             const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
             if (m != 0) {
