@@ -433,6 +433,7 @@ def run_decode(args):
         step()
     torch.cuda.synchronize()
     op.set_timing(True)
+    launches0 = op.stats()["launches"]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -442,6 +443,12 @@ def run_decode(args):
     st = op.stats()
     ms = e0.elapsed_time(e1) / args.steps
     pairs = st["visible_pairs"]
+    # a few queries against the whole cache: the key stream (S x d elements,
+    # plus the fp8 scales) is the algorithmic traffic of the filter kernel
+    peaks, kind = measured_peaks()
+    k_bytes = S * 128 * (1 if args.dtype == "fp8" else 2) + (S * 4 if args.dtype == "fp8" else 0)
+    achieved = k_bytes / (st["ms_filter"] * 1e-3) / 1e9
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     line = {"metric": DECODE_METRIC, "value": world * pairs / (ms * 1e-3), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
@@ -449,6 +456,11 @@ def run_decode(args):
             "config": {"workload": f"decode: T={T} queries at positions {S - T}..{S - 1}, S={S}, H=64, "
                                    f"d=128, k=2048, previous-step sample; keys split over the GPU",
                        "engine": args.engine},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "filter stage (key stream of the whole cache)",
+                         "peak_source": f"{kind} copy bandwidth", "algorithmic_bytes_per_call": k_bytes},
+            "gpu_launches": st["launches"] - launches0,
             "stages_ms": {"sample": st["ms_sample"], "filter": st["ms_filter"], "select": st["ms_select"]},
             "candidates_per_query": st["cand_written"] / T, "n_overflow": st["n_overflow"]}
     op.close()

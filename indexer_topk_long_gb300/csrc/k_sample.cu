@@ -11,7 +11,9 @@
 //                         the previous chunk's queries selected them;
 //   * prepare_sample   -- drops out-of-range and duplicate ids (a duplicate
 //                         would count one key twice in the sample's k-th score
-//                         and could lift the threshold above the true one);
+//                         and could lift the threshold above the true one):
+//                         the ids mark a bitmap of the key range, and one CTA
+//                         lists the set bits in ascending order;
 //   * gather_keys      -- copies the sample's key rows into a dense tile;
 //   * sample_stats     -- per query: s_min, s_max, delta and the initial
 //                         threshold bin from the scored sample.
@@ -58,47 +60,87 @@ __global__ void random_sample_kernel(long long S, int n, unsigned long long seed
 
 constexpr int kPrepThreads = 1024;
 
-// Sort the ids, keep the first copy of each valid id; the padded tail and
-// dropped ids get INT_MAX ("no key").
-__global__ void __launch_bounds__(kPrepThreads) prepare_sample_kernel(const int* ids, int n,
-                                                                      long long S, int n_pad,
-                                                                      int* key_ids_pad) {
-  extern __shared__ int sid[];
-  int P = 1;
-  while (P < n) P <<= 1;
-  for (int i = threadIdx.x; i < P; i += blockDim.x) {
-    int v = INT_MAX;
-    if (i < n) {
-      const int x = ids[i];
-      if (x >= 0 && static_cast<long long>(x) < S) v = x;
+// Set the bit of every valid id (the bitmap is all clear on entry).
+__global__ void mark_ids_kernel(const int* __restrict__ ids, int n, long long S, uint32_t* bitmap) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int x = ids[i];
+  if (x >= 0 && static_cast<long long>(x) < S) atomicOr(&bitmap[x >> 5], 1u << (x & 31));
+}
+
+// One CTA: the set bits, in ascending order, become the sample's distinct key
+// ids; the tail up to n_pad gets INT_MAX ("no key"); every word read is
+// cleared for the next call.  Warp w owns a contiguous run of words and reads
+// it 32 words per round (lane i word i), 8 rounds in flight: a popcount pass,
+// a scan of the warp totals, then the listing pass, whose positions come from
+// a warp scan of each round's popcounts.
+__global__ void __launch_bounds__(kPrepThreads) compact_ids_kernel(uint32_t* bitmap, long long words,
+                                                                   int n_pad, int* key_ids_pad) {
+  constexpr int kRounds = 8;
+  __shared__ int warp_base[kPrepThreads / 32];
+  __shared__ int total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  const long long per_w = ((words + nw - 1) / nw + 31) / 32 * 32;
+  const long long lo = static_cast<long long>(warp) * per_w;
+  const long long hi = lo + per_w < words ? lo + per_w : words;
+  int cnt = 0;
+  for (long long w0 = lo; w0 < hi; w0 += 32 * kRounds) {
+    uint32_t b[kRounds];
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const long long w = w0 + u * 32 + lane;
+      b[u] = w < hi ? bitmap[w] : 0u;
     }
-    sid[i] = v;
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) cnt += __popc(b[u]);
+  }
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+  if (lane == 0) warp_base[warp] = cnt;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nw ? warp_base[lane] : 0;
+    int sc = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, sc, o);
+      if (lane >= o) sc += u;
+    }
+    if (lane < nw) warp_base[lane] = sc - v;   // exclusive
+    if (lane == 31) total = sc;
   }
   __syncthreads();
-  // bitonic sort, ascending
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const int a = sid[lo], b = sid[hi];
-        if ((a > b) == up) {
-          sid[lo] = b;
-          sid[hi] = a;
+  int pos = warp_base[warp];
+  for (long long w0 = lo; w0 < hi; w0 += 32 * kRounds) {
+    uint32_t b[kRounds];
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const long long w = w0 + u * 32 + lane;
+      b[u] = w < hi ? bitmap[w] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kRounds; ++u) {
+      const long long w = w0 + u * 32 + lane;
+      const int c = __popc(b[u]);
+      int incl = c;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      int q = pos + incl - c;
+      if (b[u] != 0u) {
+        bitmap[w] = 0u;
+        uint32_t bb = b[u];
+        while (bb != 0u) {
+          const int bit = __ffs(bb) - 1;
+          bb &= bb - 1u;
+          if (q < n_pad) key_ids_pad[q] = static_cast<int>(w * 32 + bit);
+          ++q;
         }
       }
-      __syncthreads();
+      pos += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
   }
-  for (int r = threadIdx.x; r < n_pad; r += blockDim.x) {
-    int v = INT_MAX;
-    if (r < n) {
-      const int x = sid[r];
-      if (x != INT_MAX && (r == 0 || sid[r - 1] != x)) v = x;
-    }
-    key_ids_pad[r] = v;
-  }
+  for (int r = total + threadIdx.x; r < n_pad; r += blockDim.x) key_ids_pad[r] = INT_MAX;
 }
 
 // Copy sample rows (16-byte vectors); missing ids give zero rows.
@@ -120,32 +162,56 @@ __global__ void gather_keys_kernel(const uint4* __restrict__ k_cache, const floa
 constexpr int kStatsThreads = 256;
 
 // Block-wide radix select of the r-th largest (1-based) of m uint32 values in
-// shared memory.  Returns the value.
+// shared memory (blockDim.x a multiple of 32, at least 256).  Returns the
+// value.  Per 8-bit digit: a histogram of shared atomics (one per warp when
+// all its lanes share the digit), then the first
+// 256 threads scan the digits from the top in parallel and the one whose digit
+// holds the r-th value publishes it.
 __device__ uint32_t block_select_u32(const uint32_t* vals, int m, int r, unsigned* hist256,
-                                     uint32_t* sh_state) {
+                                     uint32_t* sh_state, unsigned* warp_tot) {
   uint32_t prefix = 0, mask = 0;
   int remaining = r;
+  const int tid = threadIdx.x, lane = tid & 31;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist256[i] = 0;
+    for (int i = tid; i < 256; i += blockDim.x) hist256[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < m; i += blockDim.x) {
-      const uint32_t v = vals[i];
-      if ((v & mask) == prefix) atomicAdd(&hist256[(v >> shift) & 255u], 1u);
+    for (int i0 = 0; i0 < m; i0 += blockDim.x) {
+      const int i = i0 + tid;
+      const uint32_t v = i < m ? vals[i] : 0u;
+      const bool in = i < m && (v & mask) == prefix;
+      const unsigned act = __ballot_sync(0xFFFFFFFFu, in);
+      if (in) {
+        // one atomic when every active lane has the same digit (the common case
+        // for the high digits of a narrow score range), else one per lane
+        const unsigned dig = (v >> shift) & 255u;
+        const int leader = __ffs(act) - 1;
+        const unsigned d0 = __shfl_sync(act, dig, leader);
+        if (__all_sync(act, dig == d0)) {
+          if (lane == leader) atomicAdd(&hist256[dig], static_cast<unsigned>(__popc(act)));
+        } else {
+          atomicAdd(&hist256[dig], 1u);
+        }
+      }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int above = 0;
-      int digit = 0;
-      for (int dgt = 255; dgt >= 0; --dgt) {
-        const int c = static_cast<int>(hist256[dgt]);
-        if (above + c >= remaining) {
-          digit = dgt;
-          break;
-        }
-        above += c;
+    unsigned c = 0, incl = 0;
+    if (tid < 256) {
+      c = hist256[255 - tid];             // thread t looks at digit 255 - t
+      incl = c;
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += u;
       }
-      sh_state[0] = static_cast<uint32_t>(digit);
-      sh_state[1] = static_cast<uint32_t>(above);
+      if (lane == 31) warp_tot[tid >> 5] = incl;
+    }
+    __syncthreads();
+    if (tid < 256) {
+      for (int w = 0; w < (tid >> 5); ++w) incl += warp_tot[w];
+      const unsigned above = incl - c;    // values with a larger digit
+      if (above < static_cast<unsigned>(remaining) && incl >= static_cast<unsigned>(remaining)) {
+        sh_state[0] = static_cast<uint32_t>(255 - tid);
+        sh_state[1] = above;
+      }
     }
     __syncthreads();
     prefix |= sh_state[0] << shift;
@@ -166,12 +232,13 @@ __device__ uint32_t block_select_u32(const uint32_t* vals, int m, int r, unsigne
 // it, and everything under the range clamps into bin 0 and is rejected.  With
 // fewer than k visible sample keys (or no spread above s_k) the bins cover
 // [s_min, s_max + (s_max - s_min)] and the threshold starts at 0.
-__global__ void __launch_bounds__(kStatsThreads) sample_stats_kernel(const SampleStatsParams p) {
+__global__ void __launch_bounds__(1024) sample_stats_kernel(const SampleStatsParams p) {
   extern __shared__ uint32_t s_ord[];
   __shared__ unsigned hist256[256];
   __shared__ uint32_t sh_state[2];
-  __shared__ float red_min[kStatsThreads / 32], red_max[kStatsThreads / 32];
-  __shared__ int red_cnt[kStatsThreads / 32];
+  __shared__ unsigned warp_tot[8];
+  __shared__ float red_min[32], red_max[32];
+  __shared__ int red_cnt[32];
   const int t = blockIdx.x;
   const float* row = p.scores + static_cast<size_t>(t) * p.ld;
   float mn = INFINITY, mx = -INFINITY;
@@ -199,7 +266,7 @@ __global__ void __launch_bounds__(kStatsThreads) sample_stats_kernel(const Sampl
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kStatsThreads / 32; ++w) {
+    for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) {
       mn = fminf(mn, red_min[w]);
       mx = fmaxf(mx, red_max[w]);
       cnt += red_cnt[w];
@@ -216,7 +283,7 @@ __global__ void __launch_bounds__(kStatsThreads) sample_stats_kernel(const Sampl
   int theta = 0;
   bool ranged = false;
   if (cnt >= p.k && p.k > 0) {
-    const float sk = unord_f32(block_select_u32(s_ord, p.n, p.k, hist256, sh_state));
+    const float sk = unord_f32(block_select_u32(s_ord, p.n, p.k, hist256, sh_state, warp_tot));
     const float span = __fsub_rn(mx, sk);
     if (span > 0.f) {
       const float hi = __fadd_rn(mx, span);
@@ -341,14 +408,12 @@ cudaError_t launch_random_sample(long long S, int n, unsigned long long seed, in
 }
 
 cudaError_t launch_prepare_sample(const int* ids, int n, long long S, int n_pad, int* key_ids_pad,
-                                  cudaStream_t stream) {
-  int P = 1;
-  while (P < n) P <<= 1;
-  const size_t smem = static_cast<size_t>(P) * sizeof(int);
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prepare_sample_kernel), kSlotPrepare,
-                                    kMaxSample * sizeof(int));
-  if (e != cudaSuccess) return e;
-  prepare_sample_kernel<<<1, kPrepThreads, smem, stream>>>(ids, n, S, n_pad, key_ids_pad);
+                                  uint32_t* bitmap, cudaStream_t stream) {
+  if (n > 0) {
+    mark_ids_kernel<<<(n + 255) / 256, 256, 0, stream>>>(ids, n, S, bitmap);
+    count_launches(1);
+  }
+  compact_ids_kernel<<<1, kPrepThreads, 0, stream>>>(bitmap, (S + 31) / 32, n_pad, key_ids_pad);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -367,13 +432,15 @@ cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int el
   return cudaGetLastError();
 }
 
-cudaError_t launch_sample_stats(const SampleStatsParams& p, cudaStream_t stream) {
+cudaError_t launch_sample_stats(const SampleStatsParams& p, int num_sms, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
+  // few queries: one wide CTA each (the per-query work is latency-bound)
+  const int threads = p.T < num_sms ? 1024 : kStatsThreads;
   const size_t smem = static_cast<size_t>(p.n) * sizeof(uint32_t);
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(sample_stats_kernel), kSlotStats,
                                     kMaxSample * sizeof(uint32_t));
   if (e != cudaSuccess) return e;
-  sample_stats_kernel<<<p.T, kStatsThreads, smem, stream>>>(p);
+  sample_stats_kernel<<<p.T, threads, smem, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -223,6 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool shared_query = nsplit > 1;   // other CTAs scan other keys of these queries
   const int t0 = qb * kTcQPB;
   const int nq = min(kTcQPB, p.T - t0);
+  // queries in each accumulator half: a half without queries is not computed,
+  // and a half with fewer than 4 runs a narrower MMA (N = 64 per query)
+  const int hq0 = min(4, nq);
+  const int hq1 = max(0, nq - 4);
+  const int n_halves = hq1 > 0 ? 2 : 1;
+  const int n_act = 4 * hq0;   // epilogue warps with work (a query in half 0)
 
   // Keys to scan: up to the largest position in the block when causal.
   long long last_row = p.rows;
@@ -274,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->k_empty[s]), 1);
     }
     for (int j = 0; j < 2; ++j) {
+      const int hq = j == 0 ? hq0 : hq1;
       mbar_init(smem_u32(&ctrl->acc_full[j]), 1);
-      mbar_init(smem_u32(&ctrl->acc_empty[j]), kEpiWarps);
+      mbar_init(smem_u32(&ctrl->acc_empty[j]), hq > 0 ? 4 * hq : 1);
     }
     mbar_init(smem_u32(&ctrl->mma_done), 1);
     mbar_fence_init();
@@ -323,14 +330,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ---------------- MMA issuer ----------------
       if (lane == 0) {
-        const uint32_t idesc = make_idesc(FP8, kTile, kN);
+        const uint32_t idesc0 = make_idesc(FP8, kTile, kTcHeads * hq0);
+        const uint32_t idesc1 = make_idesc(FP8, kTile, kTcHeads * (hq1 > 0 ? hq1 : 1));
         bool ok = mbar_wait(smem_u32(&ctrl->q_full), 0, abort_flag, p.status);
         for (int i = 0; ok && i < n_tiles; ++i) {
           const int s = i % Sh::kStages;
           if (!mbar_wait(smem_u32(&ctrl->k_full[s]), (i / Sh::kStages) & 1, abort_flag, p.status))
             break;
           tc_fence_after();
+#pragma unroll
           for (int j = 0; j < 2; ++j) {
+            if (j >= n_halves) break;   // unrolled: the MMA issue loop must stay straight-line
+            const uint32_t idesc = j == 0 ? idesc0 : idesc1;
             if (i > 0) {
               if (!mbar_wait(smem_u32(&ctrl->acc_empty[j]), (i - 1) & 1, abort_flag, p.status)) {
                 ok = false;
@@ -364,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           int prev_done = -1;
           uint64_t t_prog = globaltimer_ns();
           while (true) {
-            int done = *reinterpret_cast<volatile int*>(&ctrl->tiles_done) / kEpiWarps;
+            int done = *reinterpret_cast<volatile int*>(&ctrl->tiles_done) / n_act;
             done = __shfl_sync(0xFFFFFFFFu, done, 0);
             const int ab = __shfl_sync(0xFFFFFFFFu, *abort_flag, 0);
             if (done >= n_tiles || ab) break;
@@ -406,11 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    } else if (warp >= kEpiWarp0) {
+    } else if (warp >= kEpiWarp0 && (warp - kEpiWarp0) / 4 < hq0) {
       // ---------------- epilogue ----------------
       const int e = warp - kEpiWarp0;
       const int lq = warp & 3;               // TMEM lane quarter this warp may access
       const int qh = e >> 2;                 // this warp's query within each half
+      const int my_halves = qh < hq1 ? 2 : 1;
       const int c = lane & 3;
       const int row = lq * 32 + (lane >> 2) + 8 * c;   // key row this thread finishes
       const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
@@ -459,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool stop = false;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
+          if (j >= my_halves) break;
           bool ok = mbar_wait(acc_full0 + 8 * j, i & 1, abort_flag, p.status);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) {

@@ -31,6 +31,7 @@ struct ltk_handle {
   void* k_samp = nullptr;              // [n_pad_max, d]
   float* k_scale_samp = nullptr;       // [n_pad_max]
   int* key_ids_pad = nullptr;          // [n_pad_max]
+  uint32_t* id_bitmap = nullptr;       // [ceil(max_S / 32)] sample-id dedupe bitmap, clear between calls
   int* sample_tmp = nullptr;           // [kMaxSample]
   float* s_min = nullptr;              // [max_T]
   float* delta = nullptr;              // [max_T]
@@ -190,6 +191,7 @@ Sizes compute_sizes(const ltk_config* c) {
   b += T * s.n_pad_max * 4;                           // sample scores
   b += static_cast<unsigned long long>(s.n_pad_max) * c->dim * s.elem;   // gathered keys
   b += static_cast<unsigned long long>(s.n_pad_max) * 4 * 2;            // scales + ids
+  b += (S + 31) / 32 * 4;                             // sample-id bitmap
   b += kMaxSample * 4ull;                             // random sample ids
   b += T * 4 * 4;                                     // s_min, delta, theta0, cnt
   b += T * static_cast<unsigned long long>(c->n_bins) * 4;   // per-query histograms shared by CTAs
@@ -247,7 +249,8 @@ cudaError_t alloc(T** p, unsigned long long bytes) {
 }
 
 void free_all(ltk_handle* h) {
-  void* ptrs[] = {h->ghist, h->samp_scores, h->k_samp, h->k_scale_samp, h->key_ids_pad, h->sample_tmp,
+  void* ptrs[] = {h->ghist, h->samp_scores, h->k_samp, h->k_scale_samp, h->key_ids_pad, h->id_bitmap,
+                  h->sample_tmp,
                   h->s_min,       h->delta,   h->theta0,       h->cand,         h->cnt,
                   h->ovf,         h->rescue_scratch, h->dense, h->status,       h->ms.counts,
                   h->ms.keys,     h->ms.hist, h->ms.state,     h->io_q,         h->io_qs,
@@ -354,11 +357,14 @@ cudaError_t launch_scorer(const ltk_handle* h, int mode, const CUtensorMap& qm, 
 // waves of query blocks stay unsplit; the query blocks of a partial last wave
 // (or of a chunk smaller than one wave, e.g. decode) are split along the keys
 // into s_last ranges, chosen so that the split units fill the SMs best, with
-// at least 64 key tiles per range.
-void plan_split(int T, long long S, int num_sms, int* b_full, int* s_last) {
+// at least min_tiles key tiles per range (a filter range starts from the
+// sample's threshold, so it must not be tiny; dense scoring has no such limit)
+// and at most one range per SM.
+void plan_split(int T, long long S, int num_sms, int min_tiles, int* b_full, int* s_last) {
   const int t_blocks = (T + kTcQPB - 1) / kTcQPB;
   const long long tiles = (S + kTile - 1) / kTile;
-  const int max_s = static_cast<int>(tiles / 64 > 1 ? (tiles / 64 < 64 ? tiles / 64 : 64) : 1);
+  const long long by_tiles = tiles / min_tiles;
+  const int max_s = static_cast<int>(by_tiles > 1 ? (by_tiles < num_sms ? by_tiles : num_sms) : 1);
   *b_full = t_blocks;
   *s_last = 1;
   if (t_blocks == 0 || max_s <= 1) return;
@@ -403,13 +409,13 @@ void plan_split_cc(int T, long long S, int num_sms, int* b_full, int* s_last) {
 
 // Work plan for the handle's scorer; *queries_per_unit is how many queries one
 // unrolled unit covers (for the rows of split units).
-void plan_work(const ltk_handle* h, int T, long long S, int* b_full, int* s_last,
+void plan_work(const ltk_handle* h, int T, long long S, bool dense, int* b_full, int* s_last,
                int* queries_per_unit) {
   if (use_cc(&h->cfg)) {
     plan_split_cc(T, S, h->num_sms, b_full, s_last);
     *queries_per_unit = 1;
   } else {
-    plan_split(T, S, h->num_sms, b_full, s_last);
+    plan_split(T, S, h->num_sms, dense ? 8 : 32, b_full, s_last);
     *queries_per_unit = kTcQPB;
   }
 }
@@ -448,7 +454,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
     ids = h->sample_tmp;
   }
   const int n_pad = static_cast<int>(round_up(n_s > 0 ? n_s : 1, kTile));
-  LTK_CUDA(launch_prepare_sample(ids, n_s, a.S, n_pad, h->key_ids_pad, st));
+  LTK_CUDA(launch_prepare_sample(ids, n_s, a.S, n_pad, h->key_ids_pad, h->id_bitmap, st));
   LTK_CUDA(launch_gather_keys(a.k_cache, a.k_scale, static_cast<int>(h->elem), c.dim, h->key_ids_pad,
                               n_pad, h->k_samp, h->k_scale_samp, st));
   CUtensorMap q_map, ks_map, k_map;
@@ -475,10 +481,10 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   sp.dense = h->samp_scores;
   sp.ld = n_pad;
   sp.status = h->status;
-  plan_work(h, a.T, n_pad, &sp.b_full, &sp.s_last, &qpu);
+  plan_work(h, a.T, n_pad, true, &sp.b_full, &sp.s_last, &qpu);
   LTK_CUDA(launch_scorer(h, kModeDense, q_map, ks_map, sp, st));
   SampleStatsParams stp{h->samp_scores, n_pad, n_pad, a.T, a.k, c.n_bins, h->s_min, h->delta, h->theta0};
-  LTK_CUDA(launch_sample_stats(stp, st));
+  LTK_CUDA(launch_sample_stats(stp, h->num_sms, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
 
   // ---- Filter (Methodology step 2)
@@ -505,7 +511,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   fp.skip_key_loads = (c.debug_flags & 1) ? 1 : 0;
   fp.ghist = h->ghist;
   fp.status = h->status;
-  plan_work(h, a.T, a.S, &fp.b_full, &fp.s_last, &qpu);
+  plan_work(h, a.T, a.S, false, &fp.b_full, &fp.s_last, &qpu);
   if (!is_retrieval(&c) && fp.s_last > 1) {
     // split query blocks count and build histograms in global memory
     const size_t t_first = static_cast<size_t>(fp.b_full) * qpu;
@@ -633,6 +639,7 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
   step(alloc(reinterpret_cast<char**>(&h->k_samp), np * cfg->dim * h->elem));
   step(alloc(&h->k_scale_samp, np * 4));
   step(alloc(&h->key_ids_pad, np * 4));
+  step(alloc(&h->id_bitmap, (S + 31) / 32 * 4));
   step(alloc(&h->sample_tmp, kMaxSample * 4ull));
   step(alloc(&h->s_min, T * 4));
   step(alloc(&h->delta, T * 4));
@@ -665,6 +672,7 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(h->ovf, 0, 8);
   if (e == cudaSuccess) e = cudaMemset(h->cnt, 0, T * 4);
+  if (e == cudaSuccess) e = cudaMemset(h->id_bitmap, 0, (S + 31) / 32 * 4);
   if (e != cudaSuccess) {
     free_all(h);
     delete h;
@@ -804,7 +812,7 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
   sp.ld = S;
   sp.status = h->status;
   int qpu_d = kTcQPB;
-  plan_work(h, T, S, &sp.b_full, &sp.s_last, &qpu_d);
+  plan_work(h, T, S, true, &sp.b_full, &sp.s_last, &qpu_d);
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
   LTK_CUDA(launch_scorer(h, kModeDense, q_map, k_map, sp, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[2], st));

@@ -435,11 +435,11 @@ struct SampleStatsParams {
 cudaError_t launch_random_sample(long long S, int n, unsigned long long seed, int* out,
                                  cudaStream_t stream);
 cudaError_t launch_prepare_sample(const int* ids, int n, long long S, int n_pad, int* key_ids_pad,
-                                  cudaStream_t stream);
+                                  uint32_t* bitmap, cudaStream_t stream);
 cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int elem_bytes, int dim,
                                const int* key_ids_pad, int n_pad, void* k_samp, float* k_scale_samp,
                                cudaStream_t stream);
-cudaError_t launch_sample_stats(const SampleStatsParams& p, cudaStream_t stream);
+cudaError_t launch_sample_stats(const SampleStatsParams& p, int num_sms, cudaStream_t stream);
 
 struct MakeSampleWs {
   int* counts;                  // [max_S]
