@@ -443,6 +443,26 @@ def run_decode(args):
     st = op.stats()
     ms = e0.elapsed_time(e1) / args.steps
     pairs = st["visible_pairs"]
+    # the same call captured once in a CUDA graph and replayed (no launch gaps)
+    op.set_timing(False)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(max(args.warmup, 1)):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = e0.elapsed_time(e1) / args.steps
     # a few queries against the whole cache: the key stream (S x d elements,
     # plus the fp8 scales) is the algorithmic traffic of the filter kernel
     peaks, kind = measured_peaks()
@@ -462,7 +482,9 @@ def run_decode(args):
                          "peak_source": f"{kind} copy bandwidth", "algorithmic_bytes_per_call": k_bytes},
             "gpu_launches": st["launches"] - launches0,
             "stages_ms": {"sample": st["ms_sample"], "filter": st["ms_filter"], "select": st["ms_select"]},
-            "candidates_per_query": st["cand_written"] / T, "n_overflow": st["n_overflow"]}
+            "candidates_per_query": st["cand_written"] / T, "n_overflow": st["n_overflow"],
+            "graph": {"ms_per_step": graph_ms, "value": world * pairs / (graph_ms * 1e-3),
+                      "how": "one call captured with torch.cuda.graph, replayed back to back"}}
     op.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
