@@ -467,8 +467,19 @@ def run_decode(args):
     # plus the fp8 scales) is the algorithmic traffic of the filter kernel
     peaks, kind = measured_peaks()
     k_bytes = S * 128 * (1 if args.dtype == "fp8" else 2) + (S * 4 if args.dtype == "fp8" else 0)
-    achieved = k_bytes / (st["ms_filter"] * 1e-3) / 1e9
-    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    flop = 16384.0 * pairs                         # H * d * 2 per visible pair (one call)
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tflops = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    if args.dtype == "fp8":
+        tflops *= FP8_OVER_BF16
+    # the bound is whichever floor is higher: streaming the cache or the MMAs
+    t_hbm = k_bytes / (hbm * 1e9)
+    t_tc = flop / (tflops * 1e12)
+    sec = st["ms_filter"] * 1e-3
+    if t_hbm >= t_tc:
+        bound, achieved, peak, unit = "hbm", k_bytes / sec / 1e9, hbm, "GB/s"
+    else:
+        bound, achieved, peak, unit = "tensor", flop / sec / 1e12, tflops, "TFLOP/s"
     line = {"metric": DECODE_METRIC, "value": world * pairs / (ms * 1e-3), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
@@ -476,10 +487,11 @@ def run_decode(args):
             "config": {"workload": f"decode: T={T} queries at positions {S - T}..{S - 1}, S={S}, H=64, "
                                    f"d=128, k=2048, previous-step sample; keys split over the GPU",
                        "engine": args.engine},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "traffic": None,
-                         "kernel": "filter stage (key stream of the whole cache)",
-                         "peak_source": f"{kind} copy bandwidth", "algorithmic_bytes_per_call": k_bytes},
+                         "kernel": "filter stage (score_tc_kernel<filter>, keys split over the GPU)",
+                         "peak_source": f"{kind} " + ("copy bandwidth" if bound == "hbm" else "bf16 sustained"),
+                         "algorithmic_bytes_per_call": k_bytes, "algorithmic_flop_per_call": flop},
             "gpu_launches": st["launches"] - launches0,
             "stages_ms": {"sample": st["ms_sample"], "filter": st["ms_filter"], "select": st["ms_select"]},
             "candidates_per_query": st["cand_written"] / T, "n_overflow": st["n_overflow"],

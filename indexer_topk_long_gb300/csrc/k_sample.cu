@@ -12,8 +12,8 @@
 //   * prepare_sample   -- drops out-of-range and duplicate ids (a duplicate
 //                         would count one key twice in the sample's k-th score
 //                         and could lift the threshold above the true one):
-//                         the ids mark a bitmap of the key range, and one CTA
-//                         lists the set bits in ascending order;
+//                         the ids mark a bitmap of the key range, whose set
+//                         bits are listed in ascending order;
 //   * gather_keys      -- copies the sample's key rows into a dense tile;
 //   * sample_stats     -- per query: s_min, s_max, delta and the initial
 //                         threshold bin from the scored sample.
@@ -58,8 +58,6 @@ __global__ void random_sample_kernel(long long S, int n, unsigned long long seed
   out[i] = static_cast<int>(lo + (span > 0 ? static_cast<long long>(r % static_cast<uint64_t>(span)) : 0));
 }
 
-constexpr int kPrepThreads = 1024;
-
 // Set the bit of every valid id (the bitmap is all clear on entry).
 __global__ void mark_ids_kernel(const int* __restrict__ ids, int n, long long S, uint32_t* bitmap) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -68,79 +66,89 @@ __global__ void mark_ids_kernel(const int* __restrict__ ids, int n, long long S,
   if (x >= 0 && static_cast<long long>(x) < S) atomicOr(&bitmap[x >> 5], 1u << (x & 31));
 }
 
-// One CTA: the set bits, in ascending order, become the sample's distinct key
-// ids; the tail up to n_pad gets INT_MAX ("no key"); every word read is
-// cleared for the next call.  Warp w owns a contiguous run of words and reads
-// it 32 words per round (lane i word i), 8 rounds in flight: a popcount pass,
-// a scan of the warp totals, then the listing pass, whose positions come from
-// a warp scan of each round's popcounts.
-__global__ void __launch_bounds__(kPrepThreads) compact_ids_kernel(uint32_t* bitmap, long long words,
-                                                                   int n_pad, int* key_ids_pad) {
-  constexpr int kRounds = 8;
-  __shared__ int warp_base[kPrepThreads / 32];
-  __shared__ int total;
+// The set bits, in ascending order, become the sample's distinct key ids; the
+// tail up to n_pad gets INT_MAX ("no key"); every word read is cleared for the
+// next call.  CTA g owns words [g * 1024, (g + 1) * 1024), four per thread:
+// count_bits sums each CTA's bits, list_bits offsets each CTA by the sums of
+// the CTAs before it and each thread by a block scan.
+constexpr int kCompactThreads = 256;
+constexpr int kWordsPerCta = 4 * kCompactThreads;
+
+__device__ __forceinline__ int block_sum(int v, int* ws) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int r = 0;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) r += ws[i];
+  return r;
+}
+
+__global__ void fill_ids_kernel(int* key_ids_pad, int n_pad) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n_pad) key_ids_pad[i] = INT_MAX;
+}
+
+__global__ void __launch_bounds__(kCompactThreads) count_bits_kernel(const uint32_t* __restrict__ bitmap,
+                                                                     long long words, int* block_sums) {
+  __shared__ int ws[kCompactThreads / 32];
+  const long long w0 = static_cast<long long>(blockIdx.x) * kWordsPerCta + 4 * threadIdx.x;
+  int c = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (w0 + u < words) c += __popc(bitmap[w0 + u]);
+  const int total = block_sum(c, ws);
+  if (threadIdx.x == 0) block_sums[blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(kCompactThreads) list_bits_kernel(uint32_t* bitmap, long long words,
+                                                                    const int* __restrict__ block_sums,
+                                                                    int n_pad, int* key_ids_pad) {
+  __shared__ int ws[kCompactThreads / 32];
+  __shared__ int wsc[kCompactThreads / 32];
+  int pre = 0, all = 0;
+  for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x) {
+    const int v = block_sums[i];
+    all += v;
+    if (i < static_cast<int>(blockIdx.x)) pre += v;
+  }
+  pre = block_sum(pre, ws);
+  all = block_sum(all, ws);
+  const long long w0 = static_cast<long long>(blockIdx.x) * kWordsPerCta + 4 * threadIdx.x;
+  uint32_t b[4];
+  int c = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    b[u] = w0 + u < words ? bitmap[w0 + u] : 0u;
+    c += __popc(b[u]);
+  }
+  // exclusive scan of the per-thread counts
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nw = static_cast<int>(blockDim.x >> 5);
-  const long long per_w = ((words + nw - 1) / nw + 31) / 32 * 32;
-  const long long lo = static_cast<long long>(warp) * per_w;
-  const long long hi = lo + per_w < words ? lo + per_w : words;
-  int cnt = 0;
-  for (long long w0 = lo; w0 < hi; w0 += 32 * kRounds) {
-    uint32_t b[kRounds];
-#pragma unroll
-    for (int u = 0; u < kRounds; ++u) {
-      const long long w = w0 + u * 32 + lane;
-      b[u] = w < hi ? bitmap[w] : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kRounds; ++u) cnt += __popc(b[u]);
+  int incl = c;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
   }
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
-  if (lane == 0) warp_base[warp] = cnt;
+  if (lane == 31) wsc[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const int v = lane < nw ? warp_base[lane] : 0;
-    int sc = v;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xFFFFFFFFu, sc, o);
-      if (lane >= o) sc += u;
-    }
-    if (lane < nw) warp_base[lane] = sc - v;   // exclusive
-    if (lane == 31) total = sc;
-  }
-  __syncthreads();
-  int pos = warp_base[warp];
-  for (long long w0 = lo; w0 < hi; w0 += 32 * kRounds) {
-    uint32_t b[kRounds];
+  int wbase = 0;
+  for (int i = 0; i < warp; ++i) wbase += wsc[i];
+  int q = pre + wbase + incl - c;
 #pragma unroll
-    for (int u = 0; u < kRounds; ++u) {
-      const long long w = w0 + u * 32 + lane;
-      b[u] = w < hi ? bitmap[w] : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kRounds; ++u) {
-      const long long w = w0 + u * 32 + lane;
-      const int c = __popc(b[u]);
-      int incl = c;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += x;
-      }
-      int q = pos + incl - c;
-      if (b[u] != 0u) {
-        bitmap[w] = 0u;
-        uint32_t bb = b[u];
-        while (bb != 0u) {
-          const int bit = __ffs(bb) - 1;
-          bb &= bb - 1u;
-          if (q < n_pad) key_ids_pad[q] = static_cast<int>(w * 32 + bit);
-          ++q;
-        }
-      }
-      pos += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  for (int u = 0; u < 4; ++u) {
+    uint32_t bb = b[u];
+    if (bb == 0u) continue;
+    bitmap[w0 + u] = 0u;
+    while (bb != 0u) {
+      const int bit = __ffs(bb) - 1;
+      bb &= bb - 1u;
+      if (q < n_pad) key_ids_pad[q] = static_cast<int>((w0 + u) * 32 + bit);
+      ++q;
     }
   }
-  for (int r = total + threadIdx.x; r < n_pad; r += blockDim.x) key_ids_pad[r] = INT_MAX;
+  for (long long r = all + static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < n_pad;
+       r += static_cast<long long>(gridDim.x) * blockDim.x)
+    key_ids_pad[r] = INT_MAX;
 }
 
 // Copy sample rows (16-byte vectors); missing ids give zero rows.
@@ -232,7 +240,8 @@ __device__ uint32_t block_select_u32(const uint32_t* vals, int m, int r, unsigne
 // it, and everything under the range clamps into bin 0 and is rejected.  With
 // fewer than k visible sample keys (or no spread above s_k) the bins cover
 // [s_min, s_max + (s_max - s_min)] and the threshold starts at 0.
-__global__ void __launch_bounds__(1024) sample_stats_kernel(const SampleStatsParams p) {
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) sample_stats_kernel(const SampleStatsParams p) {
   extern __shared__ uint32_t s_ord[];
   __shared__ unsigned hist256[256];
   __shared__ uint32_t sh_state[2];
@@ -408,14 +417,26 @@ cudaError_t launch_random_sample(long long S, int n, unsigned long long seed, in
 }
 
 cudaError_t launch_prepare_sample(const int* ids, int n, long long S, int n_pad, int* key_ids_pad,
-                                  uint32_t* bitmap, cudaStream_t stream) {
+                                  uint32_t* bitmap, int* block_sums, cudaStream_t stream) {
   if (n > 0) {
     mark_ids_kernel<<<(n + 255) / 256, 256, 0, stream>>>(ids, n, S, bitmap);
     count_launches(1);
   }
-  compact_ids_kernel<<<1, kPrepThreads, 0, stream>>>(bitmap, (S + 31) / 32, n_pad, key_ids_pad);
-  count_launches(1);
+  const long long words = (S + 31) / 32;
+  const int blocks = static_cast<int>((words + kWordsPerCta - 1) / kWordsPerCta);
+  if (blocks == 0) {
+    fill_ids_kernel<<<(n_pad + 255) / 256, 256, 0, stream>>>(key_ids_pad, n_pad);
+    count_launches(1);
+    return cudaGetLastError();
+  }
+  count_bits_kernel<<<blocks, kCompactThreads, 0, stream>>>(bitmap, words, block_sums);
+  list_bits_kernel<<<blocks, kCompactThreads, 0, stream>>>(bitmap, words, block_sums, n_pad, key_ids_pad);
+  count_launches(2);
   return cudaGetLastError();
+}
+
+int prepare_sample_blocks(long long S) {
+  return static_cast<int>(((S + 31) / 32 + kWordsPerCta - 1) / kWordsPerCta);
 }
 
 cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int elem_bytes, int dim,
@@ -434,13 +455,20 @@ cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int el
 
 cudaError_t launch_sample_stats(const SampleStatsParams& p, int num_sms, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
-  // few queries: one wide CTA each (the per-query work is latency-bound)
-  const int threads = p.T < num_sms ? 1024 : kStatsThreads;
   const size_t smem = static_cast<size_t>(p.n) * sizeof(uint32_t);
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(sample_stats_kernel), kSlotStats,
-                                    kMaxSample * sizeof(uint32_t));
-  if (e != cudaSuccess) return e;
-  sample_stats_kernel<<<p.T, threads, smem, stream>>>(p);
+  cudaError_t e;
+  if (p.T < num_sms) {
+    // few queries: one wide CTA each (the per-query work is latency-bound)
+    e = ensure_smem_limit(reinterpret_cast<const void*>(sample_stats_kernel<1024>), kSlotStatsWide,
+                          kMaxSample * sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    sample_stats_kernel<1024><<<p.T, 1024, smem, stream>>>(p);
+  } else {
+    e = ensure_smem_limit(reinterpret_cast<const void*>(sample_stats_kernel<kStatsThreads>), kSlotStats,
+                          kMaxSample * sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    sample_stats_kernel<kStatsThreads><<<p.T, kStatsThreads, smem, stream>>>(p);
+  }
   count_launches(1);
   return cudaGetLastError();
 }

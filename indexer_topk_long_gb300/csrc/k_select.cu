@@ -29,6 +29,7 @@ namespace ltk {
 namespace {
 
 constexpr int kSelThreads = 512;
+constexpr int kSelThreadsWide = 1024;   // few queries: one wide CTA each
 constexpr int kBndCap = 4096;        // boundary-bin entries held in shared memory
 constexpr int kRankSelect = 1024;    // boundary bins up to this size: select by rank counting
 
@@ -54,6 +55,33 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   float r = red[0];
   for (int i = 1; i < (blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
   return r;
+}
+
+// Block-wide exclusive prefix sum of one int per thread (thread order);
+// *total gets the sum.  ws: 32 ints of shared scratch.
+__device__ __forceinline__ int block_excl_scan(int v, int* ws, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  __syncthreads();
+  if (lane == 31) ws[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int x = lane < nw ? ws[lane] : 0;
+    int sc = x;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, sc, o);
+      if (lane >= o) sc += u;
+    }
+    if (lane < nw) ws[lane] = sc - x;
+    if (lane == 31) ws[32] = sc;
+  }
+  __syncthreads();
+  *total = ws[32];
+  return ws[w] + incl - v;
 }
 
 // Descending bitonic sort of P (power of two) 64-bit keys in shared memory.
@@ -186,16 +214,122 @@ __device__ void write_sorted(unsigned long long* buf, int kk, int k, int t, int*
   }
 }
 
+// Final threshold bin of the select histogram: the highest b with
+// count(>= b) >= kk (sh[0]; sh[1] = count strictly above it; sh[0] = 0 with
+// everything but bin 0 above when no bin reaches kk), then the output slot
+// offsets of the bins above it, highest bin first: hist[b] becomes bin b's
+// start offset and cur[b] its cursor.  Bins are split into equal segments,
+// segment 0 the highest.
+//  * warp-0 form (narrow CTAs, many queries per SM): 32 segments.
+//  * block form (wide CTA, few queries): one segment per thread and block scans.
+__device__ void theta_and_offsets_warp0(int* hist, int* cur, int kk, int* sh) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = kSelBins / 32;
+    const int top = kSelBins - lane * per;
+    int seg = 0;
+    for (int b = top - per; b < top; ++b) seg += hist[b];
+    int cum = seg;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+      if (lane >= o) cum += v;
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, cum >= kk);
+    if (m == 0u) {
+      if (lane == 31) {
+        sh[0] = 0;
+        sh[1] = cum - hist[0];
+      }
+    } else if (lane == __ffs(m) - 1) {
+      int above = cum - seg;
+      int th = top - per;
+      for (int b = top - 1; b >= top - per; --b) {
+        if (above + hist[b] >= kk) {
+          th = b;
+          break;
+        }
+        above += hist[b];
+      }
+      sh[0] = th;
+      sh[1] = above;
+    }
+    if (lane == 0) {
+      sh[2] = 0;
+      sh[3] = 0;
+    }
+    __syncwarp();
+    const int theta_f = sh[0];
+    seg = 0;
+    for (int b = top - 1; b >= top - per; --b) seg += (b > theta_f) ? hist[b] : 0;
+    int incl = seg;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - seg;
+    for (int b = top - 1; b >= top - per; --b) {
+      const int h = (b > theta_f) ? hist[b] : 0;
+      hist[b] = run;
+      cur[b] = run;
+      run += h;
+    }
+  }
+  __syncthreads();
+}
+
+__device__ void theta_and_offsets_block(int* hist, int* cur, int kk, int* scan_ws, int* sh) {
+  const int per = kSelBins / static_cast<int>(blockDim.x);
+  const int top = kSelBins - static_cast<int>(threadIdx.x) * per;
+  int seg = 0;
+  for (int b = top - per; b < top; ++b) seg += hist[b];
+  int total = 0;
+  const int above0 = block_excl_scan(seg, scan_ws, &total);
+  if (threadIdx.x == 0) {
+    sh[0] = 0;
+    sh[1] = total - hist[0];
+    sh[2] = 0;
+    sh[3] = 0;
+  }
+  __syncthreads();
+  if (above0 < kk && above0 + seg >= kk) {
+    int above = above0;
+    int th = top - per;
+    for (int b = top - 1; b >= top - per; --b) {
+      if (above + hist[b] >= kk) {
+        th = b;
+        break;
+      }
+      above += hist[b];
+    }
+    sh[0] = th;
+    sh[1] = above;
+  }
+  __syncthreads();
+  const int theta_f = sh[0];
+  seg = 0;
+  for (int b = top - 1; b >= top - per; --b) seg += (b > theta_f) ? hist[b] : 0;
+  int run = block_excl_scan(seg, scan_ws, &total);
+  for (int b = top - 1; b >= top - per; --b) {
+    const int h = (b > theta_f) ? hist[b] : 0;
+    hist[b] = run;
+    cur[b] = run;
+    run += h;
+  }
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // Select stage (fused path), one CTA per query
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams p) {
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
   extern __shared__ unsigned long long sel_smem[];
   __shared__ int hist[kSelBins];
   __shared__ int cur[kSelBins];
   __shared__ unsigned hist256[256];
   __shared__ long long sh[2];
-  __shared__ float red[kSelThreads / 32];
+  __shared__ float red[32];
+  __shared__ int scan_ws[33];
   __shared__ int sh_int[4];   // theta_f, c_above, n_out, n_bnd
 
   const int t = blockIdx.x;
@@ -243,64 +377,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectParams 
     atomicAdd(&hist[bin_of(cand_score(list[i]), lo, delta, kSelBins)], 1);
   __syncthreads();
 
-  // final threshold bin: highest b with count(>= b) >= kk (warp 0, top down)
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int per = kSelBins / 32;
-    const int top = kSelBins - lane * per;
-    int seg = 0;
-    for (int b = top - per; b < top; ++b) seg += hist[b];
-    int cum = seg;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, cum, o);
-      if (lane >= o) cum += v;
-    }
-    const unsigned m = __ballot_sync(0xFFFFFFFFu, cum >= kk);
-    const int L = m ? __ffs(m) - 1 : 31;
-    if (lane == L) {
-      int above = cum - seg;
-      int th = top - per;
-      for (int b = top - 1; b >= top - per; --b) {
-        if (above + hist[b] >= kk) {
-          th = b;
-          break;
-        }
-        above += hist[b];
-      }
-      sh_int[0] = th;
-      sh_int[1] = above;   // candidates in bins strictly above th
-      sh_int[2] = 0;
-      sh_int[3] = 0;
-    }
-  }
-  __syncthreads();
+  // final threshold bin (highest b with count(>= b) >= kk), then the slot
+  // offsets of the bins above it (descending prefix sum: bins above theta_f
+  // go straight to the output, already ordered by bin; hist becomes the start
+  // offsets, cur the cursors)
+  if constexpr (THREADS >= kSelThreadsWide)
+    theta_and_offsets_block(hist, cur, kk, scan_ws, sh_int);
+  else
+    theta_and_offsets_warp0(hist, cur, kk, sh_int);
   const int theta_f = sh_int[0];
   const int c_above = min(sh_int[1], kk);
   const int r = kk - c_above;
-
-  // Bins above theta_f go straight to the output, already ordered by bin: each
-  // bin gets a slot range from a descending prefix sum of the histogram
-  // (highest bin first).  hist becomes the start offsets, cur the cursors.
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int per = kSelBins / 32;
-    const int top = kSelBins - lane * per;      // lane 0 owns the highest bins
-    int seg = 0;
-    for (int b = top - 1; b >= top - per; --b) seg += (b > theta_f) ? hist[b] : 0;
-    int incl = seg;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - seg;
-    for (int b = top - 1; b >= top - per; --b) {
-      const int h = (b > theta_f) ? hist[b] : 0;
-      hist[b] = run;
-      cur[b] = run;
-      run += h;
-    }
-  }
-  __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const unsigned long long c = list[i];
     const float s = cand_score(c);
@@ -682,13 +769,22 @@ size_t outbuf_bytes(int k) {
 
 }  // namespace
 
-cudaError_t launch_select(const SelectParams& p, cudaStream_t stream) {
+cudaError_t launch_select(const SelectParams& p, int num_sms, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
   const size_t smem = outbuf_bytes(p.k) + kBndCap * sizeof(unsigned long long);
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel), kSlotSelect,
-                                    outbuf_bytes(kMaxK) + kBndCap * sizeof(unsigned long long));
-  if (e != cudaSuccess) return e;
-  select_kernel<<<p.T, kSelThreads, smem, stream>>>(p);
+  const size_t smem_max = outbuf_bytes(kMaxK) + kBndCap * sizeof(unsigned long long);
+  cudaError_t e;
+  if (p.T < num_sms) {
+    // few queries: one wide CTA each (the per-query work is latency-bound)
+    e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel<kSelThreadsWide>), kSlotSelectWide,
+                          smem_max);
+    if (e != cudaSuccess) return e;
+    select_kernel<kSelThreadsWide><<<p.T, kSelThreadsWide, smem, stream>>>(p);
+  } else {
+    e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel<kSelThreads>), kSlotSelect, smem_max);
+    if (e != cudaSuccess) return e;
+    select_kernel<kSelThreads><<<p.T, kSelThreads, smem, stream>>>(p);
+  }
   count_launches(1);
   return cudaGetLastError();
 }

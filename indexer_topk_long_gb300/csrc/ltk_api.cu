@@ -32,6 +32,7 @@ struct ltk_handle {
   float* k_scale_samp = nullptr;       // [n_pad_max]
   int* key_ids_pad = nullptr;          // [n_pad_max]
   uint32_t* id_bitmap = nullptr;       // [ceil(max_S / 32)] sample-id dedupe bitmap, clear between calls
+  int* id_block_sums = nullptr;        // per-CTA bit counts of the bitmap listing
   int* sample_tmp = nullptr;           // [kMaxSample]
   float* s_min = nullptr;              // [max_T]
   float* delta = nullptr;              // [max_T]
@@ -191,7 +192,7 @@ Sizes compute_sizes(const ltk_config* c) {
   b += T * s.n_pad_max * 4;                           // sample scores
   b += static_cast<unsigned long long>(s.n_pad_max) * c->dim * s.elem;   // gathered keys
   b += static_cast<unsigned long long>(s.n_pad_max) * 4 * 2;            // scales + ids
-  b += (S + 31) / 32 * 4;                             // sample-id bitmap
+  b += (S + 31) / 32 * 4 + (S + 32767) / 32768 * 4 + 4;   // sample-id bitmap + per-CTA counts
   b += kMaxSample * 4ull;                             // random sample ids
   b += T * 4 * 4;                                     // s_min, delta, theta0, cnt
   b += T * static_cast<unsigned long long>(c->n_bins) * 4;   // per-query histograms shared by CTAs
@@ -250,6 +251,7 @@ cudaError_t alloc(T** p, unsigned long long bytes) {
 
 void free_all(ltk_handle* h) {
   void* ptrs[] = {h->ghist, h->samp_scores, h->k_samp, h->k_scale_samp, h->key_ids_pad, h->id_bitmap,
+                  h->id_block_sums,
                   h->sample_tmp,
                   h->s_min,       h->delta,   h->theta0,       h->cand,         h->cnt,
                   h->ovf,         h->rescue_scratch, h->dense, h->status,       h->ms.counts,
@@ -454,7 +456,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
     ids = h->sample_tmp;
   }
   const int n_pad = static_cast<int>(round_up(n_s > 0 ? n_s : 1, kTile));
-  LTK_CUDA(launch_prepare_sample(ids, n_s, a.S, n_pad, h->key_ids_pad, h->id_bitmap, st));
+  LTK_CUDA(launch_prepare_sample(ids, n_s, a.S, n_pad, h->key_ids_pad, h->id_bitmap, h->id_block_sums, st));
   LTK_CUDA(launch_gather_keys(a.k_cache, a.k_scale, static_cast<int>(h->elem), c.dim, h->key_ids_pad,
                               n_pad, h->k_samp, h->k_scale_samp, st));
   CUtensorMap q_map, ks_map, k_map;
@@ -529,7 +531,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   // ---- Select (Methodology step 3)
   SelectParams sel{h->cand, h->cnt, c.causal ? a.positions : nullptr, a.T, a.S, c.causal, h->cap,
                    a.k, a.out_idx, a.out_score, h->ovf, h->ovf + 2, h->pairs};
-  LTK_CUDA(launch_select(sel, st));
+  LTK_CUDA(launch_select(sel, h->num_sms, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[3], st));
 
   // ---- exact rescue of overflowed candidate lists (no-op when none)
@@ -640,6 +642,7 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
   step(alloc(&h->k_scale_samp, np * 4));
   step(alloc(&h->key_ids_pad, np * 4));
   step(alloc(&h->id_bitmap, (S + 31) / 32 * 4));
+  step(alloc(&h->id_block_sums, static_cast<unsigned long long>(prepare_sample_blocks(cfg->max_S) + 1) * 4));
   step(alloc(&h->sample_tmp, kMaxSample * 4ull));
   step(alloc(&h->s_min, T * 4));
   step(alloc(&h->delta, T * 4));

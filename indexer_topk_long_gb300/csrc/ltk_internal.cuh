@@ -352,13 +352,14 @@ enum SmemSlot {
   kSlotScoreTc = 0,          // 4 instantiations: + mode * 2 + fp8
   kSlotRetrieval = 4,        // 4 instantiations: + mode * 2 + relu
   kSlotScoreCc = 8,          // 4 instantiations: + mode * 2 + fp8
-  kSlotPrepare = 12,
-  kSlotStats = 13,
+  kSlotStats = 12,
+  kSlotStatsWide = 13,
   kSlotSelect = 14,
-  kSlotRowTopk = 15,
-  kSlotRescue = 16,
-  kSlotLitedsa = 17,
-  kSlotCount = 18
+  kSlotSelectWide = 15,
+  kSlotRowTopk = 16,
+  kSlotRescue = 17,
+  kSlotLitedsa = 18,
+  kSlotCount = 19
 };
 
 // Process-wide count of kernels launched by this library (ltk_api.cu).
@@ -435,7 +436,8 @@ struct SampleStatsParams {
 cudaError_t launch_random_sample(long long S, int n, unsigned long long seed, int* out,
                                  cudaStream_t stream);
 cudaError_t launch_prepare_sample(const int* ids, int n, long long S, int n_pad, int* key_ids_pad,
-                                  uint32_t* bitmap, cudaStream_t stream);
+                                  uint32_t* bitmap, int* block_sums, cudaStream_t stream);
+int prepare_sample_blocks(long long S);   // block_sums entries launch_prepare_sample needs
 cudaError_t launch_gather_keys(const void* k_cache, const float* k_scale, int elem_bytes, int dim,
                                const int* key_ids_pad, int n_pad, void* k_samp, float* k_scale_samp,
                                cudaStream_t stream);
@@ -551,7 +553,7 @@ cudaError_t launch_litedsa_pack(const int* topk, int T, int k, int G, int* union
                                 uint32_t* masks, cudaStream_t stream);
 
 // Select stage, decoupled baseline selection and overflow rescue (k_select.cu).
-cudaError_t launch_select(const SelectParams& p, cudaStream_t stream);
+cudaError_t launch_select(const SelectParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream);
 cudaError_t launch_rescue(const RescueParams& p, int rescue_rows, cudaStream_t stream);
 
