@@ -45,6 +45,9 @@ struct Shape {
   static constexpr int kKChunkBytes = kTile * 128;
   static constexpr int kKStage = kChunks * kKChunkBytes;      // 32 KB bf16 / 16 KB e4m3
   static constexpr int kStages = FP8 ? 4 : 2;
+  // stages that fit in the query rows of group 1 when it is unused (small T)
+  static constexpr int kExtraStages = 2;
+  static constexpr int kMaxStages = kStages + kExtraStages;
   static constexpr int kMaxBins = FP8 ? 2048 : 512;
   static constexpr int kBoxCols = FP8 ? 128 : 64;             // elements per 128-byte box row
 };
@@ -58,8 +61,8 @@ constexpr uint32_t kTmemCols = 512;
 
 struct __align__(8) Ctrl {
   uint64_t q_full;
-  uint64_t k_full[4];
-  uint64_t k_empty[4];
+  uint64_t k_full[6];
+  uint64_t k_empty[6];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t mma_done;
@@ -229,6 +232,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hq1 = max(0, nq - 4);
   const int n_halves = hq1 > 0 ? 2 : 1;
   const int n_act = 4 * hq0;   // epilogue warps with work (a query in half 0)
+  // with one half of queries the two TMEM accumulators alternate between tiles,
+  // so the tensor core fills one while the epilogue drains the other
+  const bool alt = n_halves == 1;
+  // The key ring: kStages stages after the query rows, plus, when query group 1
+  // is unused, kExtraStages more in its rows (a deeper ring for the
+  // cache-streaming small-T case).
+  const int ns = Sh::kStages + (alt ? Sh::kExtraStages : 0);
+  auto k_stage = [&](int st) -> uint32_t {
+    if (st < Sh::kStages) return s_k + st * Sh::kKStage;
+    const int e = st - Sh::kStages;
+    return FP8 ? s_q + kN * 128 + e * Sh::kKStage : s_q + e * Sh::kQChunkBytes + kN * 128;
+  };
 
   // Keys to scan: up to the largest position in the block when causal.
   long long last_row = p.rows;
@@ -275,12 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctrl->abort_flag = 0;
     ctrl->tiles_done = 0;
     mbar_init(smem_u32(&ctrl->q_full), 1);
-    for (int s = 0; s < Sh::kStages; ++s) {
+    for (int s = 0; s < Sh::kMaxStages; ++s) {
       mbar_init(smem_u32(&ctrl->k_full[s]), 1);
       mbar_init(smem_u32(&ctrl->k_empty[s]), 1);
     }
     for (int j = 0; j < 2; ++j) {
-      const int hq = j == 0 ? hq0 : hq1;
+      const int hq = (j == 0 || alt) ? hq0 : hq1;
       mbar_init(smem_u32(&ctrl->acc_full[j]), 1);
       mbar_init(smem_u32(&ctrl->acc_empty[j]), hq > 0 ? 4 * hq : 1);
     }
@@ -300,31 +315,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&q_map);
         tma_prefetch_desc(&k_map);
         const uint32_t qbar = smem_u32(&ctrl->q_full);
-        mbar_arrive_expect_tx(qbar, Sh::kQBytes);
-        for (int j = 0; j < 2; ++j)
+        // the query rows of the groups in use (a group without queries is skipped)
+        mbar_arrive_expect_tx(qbar, Sh::kQBytes / 2 * n_halves);
+        for (int j = 0; j < n_halves; ++j)
           for (int c = 0; c < Sh::kChunks; ++c)
             tma_load_2d(s_q + c * Sh::kQChunkBytes + j * (kN * 128), &q_map, c * Sh::kBoxCols,
                         (t0 + 4 * j) * kTcHeads, qbar);
-        int issued[Sh::kStages];
-        for (int s = 0; s < Sh::kStages; ++s) issued[s] = -1;
+        int issued[Sh::kMaxStages];
+        for (int s = 0; s < Sh::kMaxStages; ++s) issued[s] = -1;
         for (int i = 0; i < (p.skip_key_loads ? 0 : n_tiles); ++i) {
-          const int s = i % Sh::kStages;
-          if (i >= Sh::kStages &&
-              !mbar_wait(smem_u32(&ctrl->k_empty[s]), ((i / Sh::kStages) - 1) & 1, abort_flag,
-                         p.status))
+          const int s = i % ns;
+          if (i >= ns &&
+              !mbar_wait(smem_u32(&ctrl->k_empty[s]), ((i / ns) - 1) & 1, abort_flag, p.status))
             break;
           const uint32_t fb = smem_u32(&ctrl->k_full[s]);
           mbar_arrive_expect_tx(fb, Sh::kKStage);
+          const uint32_t dst = k_stage(s);
           for (int c = 0; c < Sh::kChunks; ++c)
-            tma_load_2d(s_k + s * Sh::kKStage + c * Sh::kKChunkBytes, &k_map, c * Sh::kBoxCols,
-                        (tile_lo + i) * kTile, fb);
+            tma_load_2d(dst + c * Sh::kKChunkBytes, &k_map, c * Sh::kBoxCols, (tile_lo + i) * kTile, fb);
           issued[s] = i;
         }
         if (*abort_flag) {
           // drain copies still in flight before the CTA may exit
           mbar_drain(qbar, 0);
-          for (int s = 0; s < Sh::kStages; ++s)
-            if (issued[s] >= 0) mbar_drain(smem_u32(&ctrl->k_full[s]), (issued[s] / Sh::kStages) & 1);
+          for (int s = 0; s < ns; ++s)
+            if (issued[s] >= 0) mbar_drain(smem_u32(&ctrl->k_full[s]), (issued[s] / ns) & 1);
         }
       }
     } else if (warp == 1) {
@@ -334,16 +349,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc1 = make_idesc(FP8, kTile, kTcHeads * (hq1 > 0 ? hq1 : 1));
         bool ok = mbar_wait(smem_u32(&ctrl->q_full), 0, abort_flag, p.status);
         for (int i = 0; ok && i < n_tiles; ++i) {
-          const int s = i % Sh::kStages;
-          if (!mbar_wait(smem_u32(&ctrl->k_full[s]), (i / Sh::kStages) & 1, abort_flag, p.status))
+          const int s = i % ns;
+          if (!mbar_wait(smem_u32(&ctrl->k_full[s]), (i / ns) & 1, abort_flag, p.status))
             break;
+          const uint32_t ks_base = k_stage(s);
           tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (j >= n_halves) break;   // unrolled: the MMA issue loop must stay straight-line
-            const uint32_t idesc = j == 0 ? idesc0 : idesc1;
-            if (i > 0) {
-              if (!mbar_wait(smem_u32(&ctrl->acc_empty[j]), (i - 1) & 1, abort_flag, p.status)) {
+          for (int g = 0; g < 2; ++g) {   // query group (half of the query block)
+            if (g >= n_halves) break;   // unrolled: the MMA issue loop must stay straight-line
+            const uint32_t idesc = g == 0 ? idesc0 : idesc1;
+            const int j = alt ? (i & 1) : g;      // accumulator
+            const int use = alt ? (i >> 1) : i;   // earlier tiles that used accumulator j
+            if (use > 0) {
+              if (!mbar_wait(smem_u32(&ctrl->acc_empty[j]), (use - 1) & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
               }
@@ -354,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ks = 0; ks < Sh::kKSteps; ++ks) {
               const int c = ks >> 2;
               const int kk = ks & 3;
-              const uint64_t a = smem_desc_sw128(s_k + s * Sh::kKStage + c * Sh::kKChunkBytes + kk * 32);
-              const uint64_t b = smem_desc_sw128(s_q + c * Sh::kQChunkBytes + j * (kN * 128) + kk * 32);
+              const uint64_t a = smem_desc_sw128(ks_base + c * Sh::kKChunkBytes + kk * 32);
+              const uint64_t b = smem_desc_sw128(s_q + c * Sh::kQChunkBytes + g * (kN * 128) + kk * 32);
               tc_mma<FP8>(d_tmem, a, b, idesc, ks > 0 ? 1u : 0u);
             }
             tc_commit(smem_u32(&ctrl->acc_full[j]));
@@ -470,9 +488,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (MODE == kModeDense && p.key_ids != nullptr) kid = key_ok ? p.key_ids[key] : INT_MAX;
         bool stop = false;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < 2; ++j) {   // query group j of the block
           if (j >= my_halves) break;
-          bool ok = mbar_wait(acc_full0 + 8 * j, i & 1, abort_flag, p.status);
+          const int acc = alt ? (i & 1) : j;   // accumulator holding it
+          const int use = alt ? (i >> 1) : i;
+          bool ok = mbar_wait(acc_full0 + 8 * acc, use & 1, abort_flag, p.status);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) {
             stop = true;
@@ -486,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // read the query's 64 columns of the warp's 32 lanes in four 16-lane x
           // 32-column pieces, each load in flight while the previous piece is
           // summed; the TMEM half goes back as soon as the last piece has landed
-          const uint32_t ta = tq0 + j * kN;
+          const uint32_t ta = tq0 + acc * kN;
           float c0[16], c1[16], c2[16], c3[16];
           unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;   // (+0.f, +0.f)
           tmem_ld16x256b_x4(ta, c0);
@@ -502,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld_tied(c3);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty0 + 8 * j);
+          if (lane == 0) mbar_arrive(acc_empty0 + 8 * acc);
           head_partials(b0, b1, c3, wr[j], 4);
           float I = quad_reduce(fold_pair(a0), fold_pair(a1), fold_pair(b0), fold_pair(b1), c);
           const int ql = j * 4 + qh;            // query within the CTA
