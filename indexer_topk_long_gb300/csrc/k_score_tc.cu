@@ -196,7 +196,10 @@ __device__ __forceinline__ void refresh_threshold_global(const int* grow, int nb
   }
 }
 
-template <int MODE, bool FP8>
+// ALT (launched only when every query block has at most 4 queries, i.e.
+// T <= 4): one query group whose tiles alternate between the two accumulators,
+// and a deeper key ring.  The general form computes up to two groups per tile.
+template <int MODE, bool FP8, bool ALT>
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                     const __grid_constant__ CUtensorMap k_map, const ScoreParams p) {
@@ -226,19 +229,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool shared_query = nsplit > 1;   // other CTAs scan other keys of these queries
   const int t0 = qb * kTcQPB;
   const int nq = min(kTcQPB, p.T - t0);
-  // queries in each accumulator half: a half without queries is not computed,
-  // and a half with fewer than 4 runs a narrower MMA (N = 64 per query)
-  const int hq0 = min(4, nq);
-  const int hq1 = max(0, nq - 4);
-  const int n_halves = hq1 > 0 ? 2 : 1;
-  const int n_act = 4 * hq0;   // epilogue warps with work (a query in half 0)
-  // with one half of queries the two TMEM accumulators alternate between tiles,
-  // so the tensor core fills one while the epilogue drains the other
-  const bool alt = n_halves == 1;
+  // Query groups (halves of the block) and queries per group.  General form:
+  // both groups, 4 queries each (missing queries of a partial block are
+  // computed and masked).  ALT form (T <= 4): one group of nq queries, a
+  // narrower MMA (N = 64 per query), the second group neither loaded nor
+  // computed, and the two TMEM accumulators alternating between tiles, so the
+  // tensor core fills one while the epilogue drains the other.
+  constexpr bool alt = ALT;
+  const int hq0 = ALT ? nq : 4;
+  constexpr int hq1 = ALT ? 0 : 4;
+  constexpr int n_halves = ALT ? 1 : 2;
+  const int n_act = 4 * hq0;   // epilogue warps with work (a query in group 0)
   // The key ring: kStages stages after the query rows, plus, when query group 1
   // is unused, kExtraStages more in its rows (a deeper ring for the
   // cache-streaming small-T case).
-  const int ns = Sh::kStages + (alt ? Sh::kExtraStages : 0);
+  constexpr int ns = Sh::kStages + (alt ? Sh::kExtraStages : 0);
   auto k_stage = [&](int st) -> uint32_t {
     if (st < Sh::kStages) return s_k + st * Sh::kKStage;
     const int e = st - Sh::kStages;
@@ -440,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = warp - kEpiWarp0;
       const int lq = warp & 3;               // TMEM lane quarter this warp may access
       const int qh = e >> 2;                 // this warp's query within each half
-      const int my_halves = qh < hq1 ? 2 : 1;
+      constexpr int my_halves = n_halves;
       const int c = lane & 3;
       const int row = lq * 32 + (lane >> 2) + 8 * c;   // key row this thread finishes
       const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
@@ -572,18 +577,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, bool FP8>
+template <int MODE, bool FP8, bool ALT>
 cudaError_t launch_one(const CUtensorMap& qm, const CUtensorMap& km, const ScoreParams& p,
                        cudaStream_t stream) {
   const int t_blocks = (p.T + kTcQPB - 1) / kTcQPB;
   if (t_blocks == 0) return cudaSuccess;
   const int grid = p.b_full + (t_blocks - p.b_full) * (p.s_last > 1 ? p.s_last : 1);
   const size_t smem = smem_bytes<FP8>(MODE == kModeFilter ? p.nb : 0);
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(score_tc_kernel<MODE, FP8>),
-                                    kSlotScoreTc + MODE * 2 + (FP8 ? 1 : 0),
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(score_tc_kernel<MODE, FP8, ALT>),
+                                    kSlotScoreTc + MODE * 4 + (FP8 ? 2 : 0) + (ALT ? 1 : 0),
                                     smem_bytes<FP8>(Shape<FP8>::kMaxBins));
   if (e != cudaSuccess) return e;
-  score_tc_kernel<MODE, FP8><<<grid, kThreads, smem, stream>>>(qm, km, p);
+  score_tc_kernel<MODE, FP8, ALT><<<grid, kThreads, smem, stream>>>(qm, km, p);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -599,11 +604,17 @@ int score_tc_max_bins(bool fp8) { return fp8 ? Shape<true>::kMaxBins : Shape<fal
 
 cudaError_t launch_score_tc(int mode, bool fp8, const CUtensorMap& q_map, const CUtensorMap& k_map,
                             const ScoreParams& p, cudaStream_t stream) {
-  if (mode == kModeDense)
-    return fp8 ? launch_one<kModeDense, true>(q_map, k_map, p, stream)
-               : launch_one<kModeDense, false>(q_map, k_map, p, stream);
-  return fp8 ? launch_one<kModeFilter, true>(q_map, k_map, p, stream)
-             : launch_one<kModeFilter, false>(q_map, k_map, p, stream);
+  const bool alt = p.T <= 4;   // every query block has at most one group of queries
+  if (mode == kModeDense) {
+    if (fp8) return alt ? launch_one<kModeDense, true, true>(q_map, k_map, p, stream)
+                        : launch_one<kModeDense, true, false>(q_map, k_map, p, stream);
+    return alt ? launch_one<kModeDense, false, true>(q_map, k_map, p, stream)
+               : launch_one<kModeDense, false, false>(q_map, k_map, p, stream);
+  }
+  if (fp8) return alt ? launch_one<kModeFilter, true, true>(q_map, k_map, p, stream)
+                      : launch_one<kModeFilter, true, false>(q_map, k_map, p, stream);
+  return alt ? launch_one<kModeFilter, false, true>(q_map, k_map, p, stream)
+             : launch_one<kModeFilter, false, false>(q_map, k_map, p, stream);
 }
 
 }  // namespace ltk

@@ -349,17 +349,17 @@ __host__ __device__ constexpr uint32_t make_idesc(bool fp8, int M, int N) {
 // `slot` identifies the kernel (a small distinct integer per call site).
 cudaError_t ensure_smem_limit(const void* func, int slot, size_t bytes);
 enum SmemSlot {
-  kSlotScoreTc = 0,          // 4 instantiations: + mode * 2 + fp8
-  kSlotRetrieval = 4,        // 4 instantiations: + mode * 2 + relu
-  kSlotScoreCc = 8,          // 4 instantiations: + mode * 2 + fp8
-  kSlotStats = 12,
-  kSlotStatsWide = 13,
-  kSlotSelect = 14,
-  kSlotSelectWide = 15,
-  kSlotRowTopk = 16,
-  kSlotRescue = 17,
-  kSlotLitedsa = 18,
-  kSlotCount = 19
+  kSlotScoreTc = 0,          // 8 instantiations: + mode * 4 + fp8 * 2 + alternating form
+  kSlotRetrieval = 8,        // 4 instantiations: + mode * 2 + relu
+  kSlotScoreCc = 12,         // 4 instantiations: + mode * 2 + fp8
+  kSlotStats = 16,
+  kSlotStatsWide = 17,
+  kSlotSelect = 18,
+  kSlotSelectWide = 19,
+  kSlotRowTopk = 20,
+  kSlotRescue = 21,
+  kSlotLitedsa = 22,
+  kSlotCount = 23
 };
 
 // Process-wide count of kernels launched by this library (ltk_api.cu).
