@@ -216,6 +216,11 @@ ltk_status ltk_make_sample(ltk_handle* h, const int* prev_idx, int T_prev, int k
  *   out_idx    device [T, k] int32; out_score device [T, k] fp32 (the
  *              kernel's fp32 score of each selected key).
  * 0 <= T <= max_T, 1 <= S <= max_S.  T == 0 enqueues nothing.
+ * The call neither synchronises nor allocates, so it can be captured in a CUDA
+ * graph (stream capture) and replayed: the graph reads the buffers named here
+ * at replay time, and a replay overwrites the handle's statistics like a call.
+ * Make one call on the handle outside capture first (it sets kernel
+ * attributes on the device), and keep timing off while capturing.
  */
 ltk_status ltk_indexer_topk(ltk_handle* h, const void* q, const float* q_scale,
                             const float* w, const void* k_cache, const float* k_scale,
