@@ -23,8 +23,9 @@
 //     The gate "bin >= theta" is evaluated as one compare against a per-query
 //     score threshold tau = the smallest float whose bin is >= theta (found by
 //     binary search over float order, so the two tests agree exactly).
-//   * Several CTAs scan different corpus ranges of the same query, so the
-//     candidate count is a global atomic per warp batch, and the threshold must
+//   * Several CTAs scan different corpus ranges of the same query.  Each
+//     appends to its own segment of the query's candidate list with a
+//     CTA-local count (no global atomic on the append path), and the threshold must
 //     come from all of the query's kept keys: epilogue threads count kept keys
 //     in a shared-memory histogram; at each refresh the refresh warp moves
 //     those counts (atomicExch) into a global per-query histogram and derives
@@ -97,21 +98,25 @@ __device__ float gate_tau(int theta, float s_min, float delta, int nb) {
 }
 
 // Append the passing rows of one query (whole warp; m = the warp's pass mask,
-// nonzero): one global atomic reserves the slots, every passing lane writes
-// its (score, row) record and counts it in the query's shared histogram.  Kept
-// out of line so that the epilogue's per-query loop stays small in the
-// instruction cache; it runs only for (query, 32-row) blocks with a pass.
-__device__ __noinline__ void append_passes(const ScoreParams& p, int gq, unsigned m, bool pass,
-                                           float I, int key, int* hrow, float s_min, float delta) {
+// nonzero) to this CTA's segment of the query's list: the leader reserves the
+// slots on the CTA-local count (shared memory), every passing lane writes its
+// (score, row) record and counts it in the query's shared histogram.  Entries
+// past the segment are dropped (the count still grows, which marks the
+// overflow).  Kept out of line so that the epilogue's per-query loop stays
+// small in the instruction cache; it runs only for (query, 32-row) blocks
+// with a pass.
+__device__ __noinline__ void append_passes(unsigned long long* seg, int seg_cap, int* local_cnt, unsigned m,
+                                           bool pass, float I, int key, int* hrow, float s_min, float delta,
+                                           int nb) {
   const int lane = threadIdx.x & 31;
   const int leader = __ffs(m) - 1;
   int base = 0;
-  if (lane == leader) base = atomicAdd(&p.cnt[gq], __popc(m));
+  if (lane == leader) base = atomicAdd(local_cnt, __popc(m));
   base = __shfl_sync(0xFFFFFFFFu, base, leader);
   if (pass) {
     const int slot = base + __popc(m & ((1u << lane) - 1u));
-    if (slot < p.cap) p.cand[static_cast<size_t>(gq) * p.cap + slot] = cand_pack(I, key);
-    atomicAdd(&hrow[bin_of(I, s_min, delta, p.nb)], 1);
+    if (slot < seg_cap) seg[slot] = cand_pack(I, key);
+    atomicAdd(&hrow[bin_of(I, s_min, delta, nb)], 1);
   }
 }
 
@@ -345,7 +350,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
               const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
               if (m != 0u) {
                 const QState st = qs[q];
-                append_passes(p, t0 + q, m, pass, I, key, hist + q * hstride, st.s_min, st.delta);
+                int* hrow = hist + q * hstride;
+                append_passes(p.cand + static_cast<size_t>(t0 + q) * p.cap + static_cast<size_t>(split) * p.seg_cap,
+                              p.seg_cap, hrow + p.nb, m, pass, I, key, hrow, st.s_min, st.delta, p.nb);
               }
             }
           }
@@ -385,6 +392,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kRTmemCols);
   }
+  if constexpr (MODE == kModeFilter) {
+    // this CTA's segment counts (the count sits in the pad word of the query's
+    // histogram row); an overflowed segment marks the whole query for rescue
+    for (int q = tid; q < nq; q += kRThreads) {
+      const int c = hist[q * hstride + p.nb];
+      p.seg_cnt[static_cast<size_t>(t0 + q) * p.nseg + split] = min(c, p.seg_cap);
+      if (c > p.seg_cap) p.cnt[t0 + q] = p.cap + 1;
+    }
+  }
 }
 
 template <int MODE, bool RELU>
@@ -392,14 +408,8 @@ cudaError_t launch_r(const CUtensorMap& qm, const CUtensorMap& cm, const ScorePa
                      int* ghist, int num_sms, cudaStream_t stream) {
   const int t_blocks = (p.T + kRN - 1) / kRN;
   if (t_blocks == 0) return cudaSuccess;
-  const int total_tiles = static_cast<int>((p.rows + kTile - 1) / kTile);
-  // Fill the GPU, but give every CTA at least kMinTilesPerCta corpus tiles: the
-  // threshold can only rise while a scan streams, so ranges must not be tiny.
-  constexpr int kMinTilesPerCta = 64;
-  int n_split = max(1, num_sms / t_blocks);
-  n_split = min(n_split, max(1, total_tiles / kMinTilesPerCta));
-  const int per = (total_tiles + n_split - 1) / n_split;
-  n_split = (total_tiles + per - 1) / per;
+  int n_split = 1, per = 1;
+  retrieval_split(p.T, p.rows, num_sms, &n_split, &per);
   const size_t smem = r_smem_bytes(MODE == kModeFilter ? p.nb : 0);
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(retrieval_tc_kernel<MODE, RELU>),
                                     kSlotRetrieval + MODE * 2 + (RELU ? 1 : 0),
@@ -412,6 +422,19 @@ cudaError_t launch_r(const CUtensorMap& qm, const CUtensorMap& cm, const ScorePa
 }
 
 }  // namespace
+
+// Fill the GPU, but give every CTA at least kMinTilesPerCta corpus tiles: the
+// threshold can only rise while a scan streams, so ranges must not be tiny.
+void retrieval_split(int T, long long rows, int num_sms, int* n_split, int* per) {
+  constexpr int kMinTilesPerCta = 64;
+  const int t_blocks = (T + kRN - 1) / kRN;
+  const int total_tiles = static_cast<int>((rows + kTile - 1) / kTile);
+  int ns = t_blocks > 0 ? max(1, num_sms / t_blocks) : 1;
+  ns = min(ns, max(1, total_tiles / kMinTilesPerCta));
+  const int pr = max(1, (total_tiles + ns - 1) / ns);
+  *per = pr;
+  *n_split = max(1, (total_tiles + pr - 1) / pr);
+}
 
 size_t retrieval_tc_smem_bytes(int mode, int nb) { return r_smem_bytes(mode == kModeFilter ? nb : 0); }
 

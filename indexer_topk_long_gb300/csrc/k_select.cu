@@ -162,21 +162,46 @@ __device__ unsigned long long select_u64_smem(const unsigned long long* keys, in
 
 // r-th largest composite key among the list entries whose select-bin is `bin`
 // (global-memory variant for a boundary bin too large for shared memory).
-__device__ unsigned long long select_u64_list(const unsigned long long* list, int n, float lo,
-                                              float delta, int bin, int r, unsigned* hist256,
-                                              long long* sh) {
+// A query's retained candidates: one contiguous list of n entries, or (SEG)
+// nseg segments of seg_cap entries, each with its own count (cnts, shared
+// memory), walked one segment per warp.  Callers only need every entry once,
+// in any order.
+template <bool SEG>
+struct CandList {
+  const unsigned long long* base;
+  int n;
+  const int* cnts;
+  int nseg;
+  int seg_cap;
+  template <typename F>
+  __device__ __forceinline__ void for_each(F f) const {
+    if constexpr (!SEG) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) f(base[i]);
+    } else {
+      const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+      for (int sg = w; sg < nseg; sg += nw) {
+        const unsigned long long* b = base + static_cast<size_t>(sg) * seg_cap;
+        const int c = cnts[sg];
+        for (int i = lane; i < c; i += 32) f(b[i]);
+      }
+    }
+  }
+};
+
+template <bool SEG>
+__device__ unsigned long long select_u64_list(const CandList<SEG>& L, float lo, float delta, int bin, int r,
+                                              unsigned* hist256, long long* sh) {
   unsigned long long prefix = 0, mask = 0;
   long long remaining = r;
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist256[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const unsigned long long c = list[i];
+    L.for_each([&](unsigned long long c) {
       const float s = cand_score(c);
-      if (bin_of(s, lo, delta, kSelBins) != bin) continue;
+      if (bin_of(s, lo, delta, kSelBins) != bin) return;
       const unsigned long long k = ckey(s, cand_idx(c));
       if ((k & mask) == prefix) atomicAdd(&hist256[(k >> shift) & 255u], 1u);
-    }
+    });
     __syncthreads();
     pick_digit(hist256, remaining, sh);
     prefix |= static_cast<unsigned long long>(sh[0]) << shift;
@@ -321,7 +346,9 @@ __device__ void theta_and_offsets_block(int* hist, int* cur, int kk, int* scan_w
 // ---------------------------------------------------------------------------
 // Select stage (fused path), one CTA per query
 // ---------------------------------------------------------------------------
-template <int THREADS>
+constexpr int kMaxSegs = 256;   // segments per query of a segmented list
+
+template <int THREADS, bool SEG>
 __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
   extern __shared__ unsigned long long sel_smem[];
   __shared__ int hist[kSelBins];
@@ -331,6 +358,7 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
   __shared__ float red[32];
   __shared__ int scan_ws[33];
   __shared__ int sh_int[4];   // theta_f, c_above, n_out, n_bnd
+  __shared__ int seg_s[SEG ? kMaxSegs : 1];
 
   const int t = blockIdx.x;
   const int V = visible_of(p.positions, t, p.S, p.causal);
@@ -348,8 +376,19 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
   while (P < max(kk, 1)) P <<= 1;
   unsigned long long* outbuf = sel_smem;          // [P]
   unsigned long long* bnd = sel_smem + P;         // [kBndCap]
-  const int n = n_raw;
   const unsigned long long* list = p.cand + static_cast<size_t>(t) * p.cap;
+  int n = n_raw;
+  if constexpr (SEG) {
+    int c = 0;
+    for (int i = threadIdx.x; i < p.nseg; i += blockDim.x) {
+      seg_s[i] = p.seg_cnt[static_cast<size_t>(t) * p.nseg + i];
+      c += seg_s[i];
+    }
+    int total = 0;
+    block_excl_scan(c, scan_ws, &total);
+    n = total;
+  }
+  const CandList<SEG> L{list, n, seg_s, p.nseg, p.seg_cap};
   if (kk == 0 || n == 0) {
     write_sorted(outbuf, 0, p.k, t, p.out_idx, p.out_score);
     return;
@@ -357,11 +396,11 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
 
   // pass A: range of the retained scores
   float mn = INFINITY, mx = -INFINITY;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const float s = cand_score(list[i]);
+  L.for_each([&](unsigned long long c) {
+    const float s = cand_score(c);
     mn = fminf(mn, s);
     mx = fmaxf(mx, s);
-  }
+  });
   const float lo = block_min(mn, red);
   const float hi = block_max(mx, red);
   float delta = 0.f;
@@ -373,8 +412,7 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
   // pass B: histogram of the retained list
   for (int i = threadIdx.x; i < kSelBins; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    atomicAdd(&hist[bin_of(cand_score(list[i]), lo, delta, kSelBins)], 1);
+  L.for_each([&](unsigned long long c) { atomicAdd(&hist[bin_of(cand_score(c), lo, delta, kSelBins)], 1); });
   __syncthreads();
 
   // final threshold bin (highest b with count(>= b) >= kk), then the slot
@@ -388,8 +426,7 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
   const int theta_f = sh_int[0];
   const int c_above = min(sh_int[1], kk);
   const int r = kk - c_above;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const unsigned long long c = list[i];
+  L.for_each([&](unsigned long long c) {
     const float s = cand_score(c);
     const int b = bin_of(s, lo, delta, kSelBins);
     if (b > theta_f) {
@@ -399,7 +436,7 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
       const int slot = atomicAdd(&sh_int[3], 1);
       if (slot < kBndCap) bnd[slot] = ckey(s, cand_idx(c));
     }
-  }
+  });
   __syncthreads();
   const int m_bnd = sh_int[3];
 
@@ -448,17 +485,16 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
             if (slot < kk) outbuf[slot] = bnd[i];
           }
       } else {
-        kth = select_u64_list(list, n, lo, delta, theta_f, r, hist256, sh);
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-          const unsigned long long c = list[i];
+        kth = select_u64_list(L, lo, delta, theta_f, r, hist256, sh);
+        L.for_each([&](unsigned long long c) {
           const float s = cand_score(c);
-          if (bin_of(s, lo, delta, kSelBins) != theta_f) continue;
+          if (bin_of(s, lo, delta, kSelBins) != theta_f) return;
           const unsigned long long key = ckey(s, cand_idx(c));
           if (key >= kth) {
             const int slot = atomicAdd(&sh_int[2], 1);
             if (slot < kk) outbuf[slot] = key;
           }
-        }
+        });
       }
     }
   }
@@ -769,24 +805,27 @@ size_t outbuf_bytes(int k) {
 
 }  // namespace
 
-cudaError_t launch_select(const SelectParams& p, int num_sms, cudaStream_t stream) {
-  if (p.T <= 0) return cudaSuccess;
+template <int THREADS, bool SEG>
+cudaError_t launch_select_as(const SelectParams& p, int slot, cudaStream_t stream) {
   const size_t smem = outbuf_bytes(p.k) + kBndCap * sizeof(unsigned long long);
   const size_t smem_max = outbuf_bytes(kMaxK) + kBndCap * sizeof(unsigned long long);
-  cudaError_t e;
-  if (p.T < num_sms) {
-    // few queries: one wide CTA each (the per-query work is latency-bound)
-    e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel<kSelThreadsWide>), kSlotSelectWide,
-                          smem_max);
-    if (e != cudaSuccess) return e;
-    select_kernel<kSelThreadsWide><<<p.T, kSelThreadsWide, smem, stream>>>(p);
-  } else {
-    e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel<kSelThreads>), kSlotSelect, smem_max);
-    if (e != cudaSuccess) return e;
-    select_kernel<kSelThreads><<<p.T, kSelThreads, smem, stream>>>(p);
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(select_kernel<THREADS, SEG>), slot, smem_max);
+  if (e != cudaSuccess) return e;
+  select_kernel<THREADS, SEG><<<p.T, THREADS, smem, stream>>>(p);
   count_launches(1);
   return cudaGetLastError();
+}
+
+cudaError_t launch_select(const SelectParams& p, int num_sms, cudaStream_t stream) {
+  if (p.T <= 0) return cudaSuccess;
+  if (p.seg_cnt != nullptr && (p.nseg < 1 || p.nseg > kMaxSegs)) return cudaErrorInvalidValue;
+  // few queries: one wide CTA each (the per-query work is latency-bound)
+  const bool wide = p.T < num_sms;
+  if (p.seg_cnt != nullptr)
+    return wide ? launch_select_as<kSelThreadsWide, true>(p, kSlotSelectSegWide, stream)
+                : launch_select_as<kSelThreads, true>(p, kSlotSelectSeg, stream);
+  return wide ? launch_select_as<kSelThreadsWide, false>(p, kSlotSelectWide, stream)
+              : launch_select_as<kSelThreads, false>(p, kSlotSelect, stream);
 }
 
 cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream) {

@@ -41,6 +41,8 @@ struct ltk_handle {
   int* cnt = nullptr;                  // [max_T]
   int* ovf = nullptr;                  // [2 + max_T]: count, next, list
   int* ghist = nullptr;                // [max_T, n_bins] per-query histograms shared by CTAs
+  int* seg_cnt = nullptr;              // [max_T, num_sms] segment counts (retrieval lists)
+  int last_nseg = 0;                   // segments per query list of the last fused call (0: one list)
   float* rescue_scratch = nullptr;     // [rescue_rows, max_S]
   float* dense = nullptr;              // [max_T, max_S] (decoupled baseline)
   int* status = nullptr;               // [1]
@@ -196,6 +198,7 @@ Sizes compute_sizes(const ltk_config* c) {
   b += kMaxSample * 4ull;                             // random sample ids
   b += T * 4 * 4;                                     // s_min, delta, theta0, cnt
   b += T * static_cast<unsigned long long>(c->n_bins) * 4;   // per-query histograms shared by CTAs
+  if (is_retrieval(c)) b += T * 256ull * 4;           // segment counts (at most one segment per SM)
   b += T * static_cast<unsigned long long>(s.cap) * 8;  // candidate lists
   b += (T + 2) * 4;                                   // overflow list
   b += static_cast<unsigned long long>(s.rescue_rows) * S * 4;   // rescue rows
@@ -251,7 +254,7 @@ cudaError_t alloc(T** p, unsigned long long bytes) {
 
 void free_all(ltk_handle* h) {
   void* ptrs[] = {h->ghist, h->samp_scores, h->k_samp, h->k_scale_samp, h->key_ids_pad, h->id_bitmap,
-                  h->id_block_sums,
+                  h->id_block_sums, h->seg_cnt,
                   h->sample_tmp,
                   h->s_min,       h->delta,   h->theta0,       h->cand,         h->cnt,
                   h->ovf,         h->rescue_scratch, h->dense, h->status,       h->ms.counts,
@@ -521,7 +524,15 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
     LTK_CUDA(cudaMemsetAsync(h->cnt + t_first, 0, n * sizeof(int), st));
     LTK_CUDA(cudaMemsetAsync(h->ghist + t_first * c.n_bins, 0, n * c.n_bins * sizeof(int), st));
   }
+  h->last_nseg = 0;
   if (is_retrieval(&c)) {
+    // each corpus range appends to its own segment of the query's list
+    int n_split = 1, per = 1;
+    retrieval_split(a.T, a.S, h->num_sms, &n_split, &per);
+    fp.seg_cnt = h->seg_cnt;
+    fp.nseg = n_split;
+    fp.seg_cap = h->cap / n_split;
+    h->last_nseg = n_split;
     LTK_CUDA(cudaMemsetAsync(h->cnt, 0, static_cast<size_t>(a.T) * sizeof(int), st));
     LTK_CUDA(cudaMemsetAsync(h->ghist, 0, static_cast<size_t>(a.T) * c.n_bins * sizeof(int), st));
   }
@@ -530,7 +541,8 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
 
   // ---- Select (Methodology step 3)
   SelectParams sel{h->cand, h->cnt, c.causal ? a.positions : nullptr, a.T, a.S, c.causal, h->cap,
-                   a.k, a.out_idx, a.out_score, h->ovf, h->ovf + 2, h->pairs};
+                   a.k, a.out_idx, a.out_score, h->ovf, h->ovf + 2, h->pairs,
+                   fp.seg_cnt, fp.nseg, fp.seg_cap};
   LTK_CUDA(launch_select(sel, h->num_sms, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[3], st));
 
@@ -648,6 +660,7 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
   step(alloc(&h->delta, T * 4));
   step(alloc(&h->theta0, T * 4));
   step(alloc(&h->ghist, T * static_cast<unsigned long long>(cfg->n_bins) * 4));
+  if (is_retrieval(cfg)) step(alloc(&h->seg_cnt, T * static_cast<unsigned long long>(h->num_sms) * 4));
   step(alloc(&h->cand, T * static_cast<unsigned long long>(h->cap) * 8));
   step(alloc(&h->cnt, T * 4));
   step(alloc(&h->ovf, (T + 2) * 4));
@@ -860,6 +873,27 @@ ltk_status ltk_get_stats(ltk_handle* h, ltk_stats* out) {
     if (e != cudaSuccess) {
       std::free(cnt);
       return cuda_fail(e, "stats");
+    }
+    if (h->last_nseg > 0) {
+      // segmented lists: a query's count is the sum of its segments' counts
+      const size_t ns = static_cast<size_t>(h->last_T) * h->last_nseg;
+      int* seg = static_cast<int*>(std::malloc(ns * 4));
+      if (seg == nullptr) {
+        std::free(cnt);
+        return LTK_ERR_NOMEM;
+      }
+      e = cudaMemcpy(seg, h->seg_cnt, ns * 4, cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) {
+        std::free(seg);
+        std::free(cnt);
+        return cuda_fail(e, "stats");
+      }
+      for (int i = 0; i < h->last_T; ++i) {
+        long long c = 0;
+        for (int j = 0; j < h->last_nseg; ++j) c += seg[static_cast<size_t>(i) * h->last_nseg + j];
+        if (cnt[i] <= h->cap) cnt[i] = static_cast<int>(c);
+      }
+      std::free(seg);
     }
     long long sum = 0;
     int mx = 0;

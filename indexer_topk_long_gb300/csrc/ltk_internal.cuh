@@ -359,7 +359,9 @@ enum SmemSlot {
   kSlotRowTopk = 20,
   kSlotRescue = 21,
   kSlotLitedsa = 22,
-  kSlotCount = 23
+  kSlotSelectSeg = 23,
+  kSlotSelectSegWide = 24,
+  kSlotCount = 25
 };
 
 // Process-wide count of kernels launched by this library (ltk_api.cu).
@@ -395,6 +397,13 @@ struct ScoreParams {
   int b_full;
   int s_last;
   int* ghist;
+  // Segmented lists (retrieval scorer): query t's list holds nseg segments of
+  // seg_cap entries, segment s written only by the CTA scanning range s with
+  // a CTA-local count; seg_cnt [T, nseg] receives the counts, and cnt[t] is
+  // set to cap + 1 when a segment overflowed.  Null: one list per query.
+  int* seg_cnt;
+  int nseg;
+  int seg_cap;
   // raw operand pointers (the CUDA-core scorer reads q and keys directly)
   const void* q_raw;
   const void* k_raw;
@@ -419,6 +428,9 @@ cudaError_t launch_retrieval_tc(int mode, const CUtensorMap& q_map, const CUtens
                                 const ScoreParams& p, int dim, int relu, int* ghist,
                                 int num_sms, cudaStream_t stream);
 size_t retrieval_tc_smem_bytes(int mode, int nb);
+// Corpus ranges per query block of the retrieval scorer (its CTAs per block)
+// and tiles per range.
+void retrieval_split(int T, long long rows, int num_sms, int* n_split, int* per);
 
 struct SampleStatsParams {
   const float* scores;     // [T, ld] sample scores (-inf = invisible)
@@ -455,7 +467,7 @@ cudaError_t launch_make_sample(const int* prev_idx, long long n_prev, long long 
 
 struct SelectParams {
   const unsigned long long* cand;  // [T, cap]
-  const int* cnt;                  // [T]
+  const int* cnt;                  // [T] (segmented lists: 0, or cap + 1 on overflow)
   const int* positions;            // [T] or null
   int T;
   long long S;
@@ -467,6 +479,9 @@ struct SelectParams {
   int* ovf_count;
   int* ovf_list;                   // [T]
   unsigned long long* pairs;       // visible pairs of the call (accumulated)
+  const int* seg_cnt;              // [T, nseg] segment counts, or null (one list per query)
+  int nseg;
+  int seg_cap;
 };
 
 struct RowTopkParams {
