@@ -3,16 +3,21 @@
 // list for joint attention, with per-query masks that keep each token's own
 // top-k membership).
 //
-// One CTA per group of G consecutive queries:
+// One CTA of 1024 threads per group of G consecutive queries:
 //   1. the group's G * k selected indices become 64-bit keys
-//      (index << 8 | query-within-group); invalid slots (-1) sort last;
-//   2. a bitonic sort in shared memory orders them by index;
-//   3. one block-wide scan over "first occurrence of an index" flags gives
-//      every key its position j in the ascending union; the first occurrence
-//      writes union[j], and every occurrence sets bit j of its query's mask
-//      (shared-memory atomicOr);
+//      (index << 8 | query-within-group); invalid slots (-1) and the padding
+//      up to P = E * 1024 keys (E a power of two, 1..16) sort last;
+//   2. a bitonic sort with the keys in registers: thread t holds keys
+//      [t E, t E + E); exchanges at strides below E stay in the thread, strides
+//      up to 32 E go through warp shuffles, and only the longer strides go
+//      through shared memory (stored element-major, so every access is
+//      conflict-free);
+//   3. a key starts a run when its index differs from the previous key's; a
+//      block scan of the per-thread run counts gives every key its position j
+//      in the ascending union; the first key of a run writes union[j], and
+//      every key sets bit j of its query's mask (shared-memory atomicOr);
 //   4. lengths, the -1 padding of the union and the masks go to device memory.
-// G * k <= 16384 keeps the sort in shared memory (128 KB of keys).
+// G * k <= 16384.
 #include "ltk_internal.cuh"
 
 namespace ltk {
@@ -20,110 +25,240 @@ namespace {
 
 constexpr int kLdThreads = 1024;
 constexpr int kLdMaxEntries = 16384;
+template <typename K>
+__device__ __forceinline__ K shfl_xor_key(K v, int m) {
+  if constexpr (sizeof(K) == 4) {
+    return __shfl_xor_sync(0xFFFFFFFFu, v, m);
+  } else {
+    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), m);
+    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), m);
+    return (static_cast<K>(hi) << 32) | lo;
+  }
+}
+template <typename K>
+__device__ __forceinline__ K shfl_up_key(K v) {
+  if constexpr (sizeof(K) == 4) {
+    return __shfl_up_sync(0xFFFFFFFFu, v, 1);
+  } else {
+    const uint32_t lo = __shfl_up_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), 1);
+    const uint32_t hi = __shfl_up_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), 1);
+    return (static_cast<K>(hi) << 32) | lo;
+  }
+}
+template <typename K>
+__device__ __forceinline__ K kmin(K a, K b) { return a < b ? a : b; }
+template <typename K>
+__device__ __forceinline__ K kmax(K a, K b) { return a < b ? b : a; }
 
+// In-thread steps of one bitonic merge: pairs (e, e ^ M) with M = size - 1
+// (the mirrored first step, MIRROR) or (e, e + S) (the following steps), both
+// ascending: the lower slot takes the minimum.
+template <int E, int S, bool MIRROR, typename K>
+__device__ __forceinline__ void ld_in_thread(K (&v)[E]) {
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if ((e & S) == 0) {
+      const int f = MIRROR ? (e ^ (2 * S - 1)) : (e + S);
+      const K a = v[e], b = v[f];
+      v[e] = kmin(a, b);
+      v[f] = kmax(a, b);
+    }
+  }
+}
+
+template <int E, bool MIRROR, typename K>
+__device__ __forceinline__ void ld_in_thread_at(K (&v)[E], int half) {
+  switch (half) {
+    case 1: ld_in_thread<E, 1, MIRROR>(v); break;
+    case 2: if constexpr (E > 2) ld_in_thread<E, 2, MIRROR>(v); break;
+    case 4: if constexpr (E > 4) ld_in_thread<E, 4, MIRROR>(v); break;
+    case 8: if constexpr (E > 8) ld_in_thread<E, 8, MIRROR>(v); break;
+    default: break;
+  }
+}
+
+// Ascending bitonic sort of E * blockDim keys, thread t holding keys
+// [t E, t E + E).  Each merge of blocks of `size` keys starts with the mirrored
+// step (key i against key i ^ (size - 1)) and continues with half strides, so
+// every exchange is ascending and needs no direction: the lower index keeps
+// the minimum.  Strides below E stay in the thread, strides below 32 E use warp
+// shuffles, longer ones the shared-memory buffer xs, stored slot-major
+// (xs[e * blockDim + t]) so that every access is conflict-free.
+template <int E, typename K>
+__device__ void ld_sort(K (&v)[E], K* xs) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nt = blockDim.x;
+  const int P = E * nt;
+#pragma unroll 1
+  for (int size = 2; size <= P; size <<= 1) {
+#pragma unroll 1
+    for (int half = size >> 1; half > 0; half >>= 1) {
+      const bool mirror = half == (size >> 1);
+      if (half < E) {
+        if constexpr (E > 1) {
+          if (mirror) ld_in_thread_at<E, true>(v, half);
+          else ld_in_thread_at<E, false>(v, half);
+        }
+      } else if (half < 32 * E) {
+        const int lm = mirror ? (size / E - 1) : (half / E);   // partner lane: lane ^ lm
+        const bool lower = (lane & (half / E)) == 0;
+        if (mirror) {
+          K o[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[e] = shfl_xor_key(v[E - 1 - e], lm);   // partner slot E-1-e
+#pragma unroll
+          for (int e = 0; e < E; ++e) v[e] = lower ? kmin(v[e], o[e]) : kmax(v[e], o[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const K o = shfl_xor_key(v[e], lm);
+            v[e] = lower ? kmin(v[e], o) : kmax(v[e], o);
+          }
+        }
+      } else {
+        const int tm = mirror ? (size / E - 1) : (half / E);   // partner thread: tid ^ tm
+        const bool lower = (tid & (half / E)) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) xs[e * nt + tid] = v[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const K o = xs[(mirror ? E - 1 - e : e) * nt + (tid ^ tm)];
+          v[e] = lower ? kmin(v[e], o) : kmax(v[e], o);
+        }
+        __syncthreads();
+      }
+    }
+  }
+}
+
+// Pack one group with keys of type K: index << 8 | query-within-group, none =
+// all ones (sorts last).
+template <int E, typename K>
+__device__ void ld_pack_group(const int* __restrict__ topk, int k, int G, int W, int t0, int ng, int g,
+                              K* xs, uint32_t* smask, int* warp_sum, K* warp_last, int* total_starts,
+                              int* union_idx, int* union_len, uint32_t* masks) {
+  constexpr K kNone = static_cast<K>(~static_cast<K>(0));
+  const int n = ng * k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  const int base = tid * E;
+  K v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = base + e;
+    K key = kNone;
+    if (i < n) {
+      const int idx = topk[static_cast<size_t>(t0) * k + i];
+      if (idx >= 0) key = (static_cast<K>(idx) << 8) | static_cast<K>(i / k);
+    }
+    v[e] = key;
+  }
+  ld_sort<E, K>(v, xs);
+
+  // the key before this thread's first key: the previous lane's last, or for
+  // lane 0 the previous warp's last
+  K prev = shfl_up_key(v[E - 1]);
+  if (lane == 31) warp_last[warp] = v[E - 1];
+  __syncthreads();
+  if (lane == 0) prev = warp > 0 ? warp_last[warp - 1] : kNone;
+  int cnt = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const K before = e == 0 ? prev : v[e - 1];
+    cnt += (v[e] != kNone && (base + e == 0 || (before >> 8) != (v[e] >> 8))) ? 1 : 0;
+  }
+  int incl = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int x = lane < nw ? warp_sum[lane] : 0;
+    int sc = x;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, sc, o);
+      if (lane >= o) sc += u;
+    }
+    if (lane < nw) warp_sum[lane] = sc - x;
+    if (lane == 31) *total_starts = sc;
+  }
+  __syncthreads();
+  int cur = warp_sum[warp] + incl - cnt - 1;   // the run before this thread's first key
+  int* urow = union_idx + static_cast<size_t>(g) * G * k;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const K key = v[e];
+    if (key == kNone) break;
+    const K before = e == 0 ? prev : v[e - 1];
+    if (base + e == 0 || (before >> 8) != (key >> 8)) {
+      ++cur;
+      urow[cur] = static_cast<int>(key >> 8);
+    }
+    const int r = static_cast<int>(key & static_cast<K>(0xFF));
+    atomicOr(&smask[r * W + (cur >> 5)], 1u << (cur & 31));
+  }
+  __syncthreads();
+  const int len = *total_starts;
+  if (tid == 0) union_len[g] = len;
+  for (int i = len + tid; i < G * k; i += blockDim.x) urow[i] = -1;
+  for (int i = tid; i < ng * W; i += blockDim.x) masks[static_cast<size_t>(t0) * W + i] = smask[i];
+}
+
+template <int E>
 __global__ void __launch_bounds__(kLdThreads)
     litedsa_pack_kernel(const int* __restrict__ topk, int T, int k, int G, int W, int* union_idx,
                         int* union_len, uint32_t* masks) {
-  extern __shared__ unsigned long long ld_keys[];
+  extern __shared__ unsigned long long ld_xs[];                  // [E * 1024] exchange
+  uint32_t* smask = reinterpret_cast<uint32_t*>(ld_xs + E * kLdThreads);   // [G][W]
   __shared__ int warp_sum[kLdThreads / 32];
+  __shared__ unsigned long long warp_last[kLdThreads / 32];
   __shared__ int total_starts;
   const int g = blockIdx.x;
   const int t0 = g * G;
   const int ng = min(G, T - t0);
-  const int n = ng * k;
-  int P = 1;
-  while (P < n) P <<= 1;
-  uint32_t* smask = reinterpret_cast<uint32_t*>(ld_keys + P);   // [G][W]
-  const unsigned long long kNone = ~0ull;
-
-  for (int e = threadIdx.x; e < P; e += blockDim.x) {
-    unsigned long long key = kNone;
-    if (e < n) {
-      const int idx = topk[static_cast<size_t>(t0) * k + e];
-      if (idx >= 0) key = (static_cast<unsigned long long>(idx) << 8) | static_cast<unsigned>(e / k);
-    }
-    ld_keys[e] = key;
-  }
   for (int i = threadIdx.x; i < G * W; i += blockDim.x) smask[i] = 0u;
-  __syncthreads();
+  // 32-bit keys when every index of the group is below 2^24 (the common case:
+  // half the exchange work of 64-bit keys, single-instruction min and max)
+  bool big = false;
+  for (int i = threadIdx.x; i < ng * k; i += blockDim.x) big |= topk[static_cast<size_t>(t0) * k + i] >= (1 << 24);
+  if (__syncthreads_or(big ? 1 : 0))
+    ld_pack_group<E, unsigned long long>(topk, k, G, W, t0, ng, g, ld_xs, smask, warp_sum, warp_last,
+                                         &total_starts, union_idx, union_len, masks);
+  else
+    ld_pack_group<E, uint32_t>(topk, k, G, W, t0, ng, g, reinterpret_cast<uint32_t*>(ld_xs), smask,
+                               warp_sum, reinterpret_cast<uint32_t*>(warp_last), &total_starts, union_idx,
+                               union_len, masks);
+}
 
-  // bitonic sort, ascending
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const unsigned long long a = ld_keys[lo], b = ld_keys[hi];
-        if ((a > b) == up) {
-          ld_keys[lo] = b;
-          ld_keys[hi] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-
-  // each thread owns a contiguous segment of the sorted keys
-  const int per = (P + blockDim.x - 1) / blockDim.x;
-  const int lo = threadIdx.x * per;
-  const int hi = min(P, lo + per);
-  auto is_start = [&](int i) {
-    const unsigned long long key = ld_keys[i];
-    if (key == kNone) return false;
-    return i == 0 || (ld_keys[i - 1] >> 8) != (key >> 8);
-  };
-  int cnt = 0;
-  for (int i = lo; i < hi; ++i) cnt += is_start(i) ? 1 : 0;
-  // exclusive scan of the per-thread counts
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = cnt;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_sum[warp] = incl;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
-      const int v = warp_sum[w];
-      warp_sum[w] = run;
-      run += v;
-    }
-    total_starts = run;
-  }
-  __syncthreads();
-  int j = warp_sum[warp] + incl - cnt - 1;   // position of the run before this segment
-  int* urow = union_idx + static_cast<size_t>(g) * G * k;
-  for (int i = lo; i < hi; ++i) {
-    const unsigned long long key = ld_keys[i];
-    if (key == kNone) break;
-    if (is_start(i)) {
-      ++j;
-      urow[j] = static_cast<int>(key >> 8);
-    }
-    const int r = static_cast<int>(key & 0xFFu);
-    atomicOr(&smask[r * W + (j >> 5)], 1u << (j & 31));
-  }
-  __syncthreads();
-  const int len = total_starts;
-  if (threadIdx.x == 0) union_len[g] = len;
-  for (int i = len + threadIdx.x; i < G * k; i += blockDim.x) urow[i] = -1;
-  for (int i = threadIdx.x; i < ng * W; i += blockDim.x)
-    masks[static_cast<size_t>(t0) * W + i] = smask[i];
+int ld_elems(int G, int k) {
+  int E = 1;
+  while (E * kLdThreads < G * k) E <<= 1;
+  return E;
 }
 
 }  // namespace
 
 int litedsa_max_entries() { return kLdMaxEntries; }
 
-// Shared memory of one group: the sorted keys (next power of two of G * k) and
-// the G masks of ceil(G * k / 32) words.
+// Shared memory of one group: the exchange buffer of the sort (E * 1024 keys)
+// and the G masks of ceil(G * k / 32) words.
 size_t litedsa_smem_bytes(int G, int k) {
-  int P = 1;
-  while (P < G * k) P <<= 1;
-  return static_cast<size_t>(P) * 8 + static_cast<size_t>(G) * ((G * k + 31) / 32) * 4;
+  return static_cast<size_t>(ld_elems(G, k)) * kLdThreads * 8 + static_cast<size_t>(G) * ((G * k + 31) / 32) * 4;
+}
+
+template <int E>
+cudaError_t launch_ld(const int* topk, int T, int k, int G, int W, int* union_idx, int* union_len,
+                      uint32_t* masks, int n_groups, size_t smem, cudaStream_t stream) {
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(litedsa_pack_kernel<E>),
+                                    kSlotLitedsa + (E == 1 ? 0 : E == 2 ? 1 : E == 4 ? 2 : E == 8 ? 3 : 4),
+                                    kLitedsaMaxSmem);
+  if (e != cudaSuccess) return e;
+  litedsa_pack_kernel<E><<<n_groups, kLdThreads, smem, stream>>>(topk, T, k, G, W, union_idx, union_len, masks);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_litedsa_pack(const int* topk, int T, int k, int G, int* union_idx, int* union_len,
@@ -132,13 +267,14 @@ cudaError_t launch_litedsa_pack(const int* topk, int T, int k, int G, int* union
   if (n_groups == 0) return cudaSuccess;
   const int W = (G * k + 31) / 32;
   const size_t smem = litedsa_smem_bytes(G, k);
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(litedsa_pack_kernel), kSlotLitedsa,
-                                    kLitedsaMaxSmem);
-  if (e != cudaSuccess) return e;
-  litedsa_pack_kernel<<<n_groups, kLdThreads, smem, stream>>>(topk, T, k, G, W, union_idx, union_len,
-                                                              masks);
-  count_launches(1);
-  return cudaGetLastError();
+  switch (ld_elems(G, k)) {
+    case 1: return launch_ld<1>(topk, T, k, G, W, union_idx, union_len, masks, n_groups, smem, stream);
+    case 2: return launch_ld<2>(topk, T, k, G, W, union_idx, union_len, masks, n_groups, smem, stream);
+    case 4: return launch_ld<4>(topk, T, k, G, W, union_idx, union_len, masks, n_groups, smem, stream);
+    case 8: return launch_ld<8>(topk, T, k, G, W, union_idx, union_len, masks, n_groups, smem, stream);
+    case 16: return launch_ld<16>(topk, T, k, G, W, union_idx, union_len, masks, n_groups, smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace ltk

@@ -358,10 +358,10 @@ enum SmemSlot {
   kSlotSelectWide = 19,
   kSlotRowTopk = 20,
   kSlotRescue = 21,
-  kSlotLitedsa = 22,
-  kSlotSelectSeg = 23,
-  kSlotSelectSegWide = 24,
-  kSlotCount = 25
+  kSlotSelectSeg = 22,
+  kSlotSelectSegWide = 23,
+  kSlotLitedsa = 24,         // 5 instantiations: keys per thread 1, 2, 4, 8, 16
+  kSlotCount = 29
 };
 
 // Process-wide count of kernels launched by this library (ltk_api.cu).

@@ -40,3 +40,22 @@ def test_packs_real_indexer_output():
     lens = _compare(idx.cpu().numpy(), 8)
     # neighbouring queries share most of their keys: far fewer list entries
     assert lens.sum() < 0.5 * 32 * 2048
+
+
+@pytest.mark.parametrize("T,k,G", [(24, 1024, 8), (6, 4, 3)])
+def test_large_indices_use_wide_keys(T, k, G):
+    """Indices of 2^24 and above take the 64-bit key path; mixed groups too."""
+    rng = np.random.default_rng(7 + k)
+    pool = rng.choice(np.arange((1 << 24) - 4 * k, (1 << 31) - 1, dtype=np.int64), size=3 * k, replace=False)
+    idx = np.stack([rng.choice(pool, size=k, replace=False) for _ in range(T)])
+    idx[: T // 2] %= (1 << 24)                       # first half of the groups: small indices only
+    idx[rng.random(idx.shape) < 0.05] = -1
+    _compare(idx, G)
+
+
+def test_full_groups_of_16384_keys():
+    """G * k = 16384 (the largest group): duplicates across all eight queries."""
+    rng = np.random.default_rng(99)
+    pool = rng.choice(1 << 20, size=3000, replace=False)
+    idx = np.stack([rng.choice(pool, size=2048, replace=False) for _ in range(16)])
+    _compare(idx, 8)
