@@ -107,10 +107,15 @@ RETRIEVAL_SOURCES = ["indexer_topk_long_gb300/csrc/k_retrieval_tc.cu", "indexer_
 
 
 def kernel_source_hash(sources=None) -> str:
+    """Hash of the kernel's code (comments and blank space removed, so that a
+    documentation edit does not retire a recorded measurement)."""
     h = hashlib.sha256()
     for rel in sources or SCORE_TC_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

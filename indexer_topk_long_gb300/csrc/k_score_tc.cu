@@ -8,24 +8,29 @@
 // an otherwise idle warp recomputes the threshold bin from the top of the
 // histogram with a plain overwrite ("Threshold Refresh").
 //
-// GB300 design (one CTA per 8 queries, 12 warps):
+// GB300 design (one CTA per work unit = 8 queries x a key range, 19 warps):
 //   * Q tile: 8 queries x 64 heads x d=128 stays resident in shared memory
 //     (bf16 128 KB, e4m3 64 KB), loaded once by TMA with 128-byte swizzle.
 //   * K tiles of 128 keys stream through a TMA ring (bf16 2 x 32 KB, e4m3
 //     4 x 16 KB).
-//   * tcgen05.mma, cta_group::1, M = 128 keys, N = 256 = 4 queries x 64 heads:
-//     keys sit on TMEM lanes, so one epilogue thread owns one key row and the
-//     weighted head sum is intra-thread.  TMEM (512 columns) holds two
-//     accumulators, one per half of the query block; the epilogue drains one
-//     half while the tensor core fills the other.
-//   * Epilogue (16 warps, one per TMEM lane quarter and query of a half):
-//     tcgen05.ld (16x256b) of the query's 64 columns, release of the TMEM half
-//     right after the load, then ReLU and the w-weighted head sum with the
-//     weights in registers (packed fp32x2 FMA, quad reduce-scatter) -> mask ->
-//     [dense: store I] or [filter: bin, gate, warp ballot append,
-//     shared-memory histogram].
+//   * tcgen05.mma, cta_group::1, M = 128 keys, N = 256 = 4 queries x 64 heads
+//     (one query group, half of the block): keys sit on TMEM lanes.  TMEM (512
+//     columns) holds two accumulators, one per group; the epilogue drains one
+//     while the tensor core fills the other.
+//   * Epilogue (16 warps, one per TMEM lane quarter and query of a group): the
+//     query's 64 columns come in four tcgen05.ld 16x256b.x4 pieces, each in
+//     flight while the previous one is summed, and the accumulator goes back
+//     once the last piece has landed; ReLU and the w-weighted head sum run as
+//     packed fp32x2 FMAs with the weights in registers, a quad reduce-scatter
+//     leaves each thread one key -> mask -> [dense: store I] or [filter: bin,
+//     gate, warp ballot append, shared-memory histogram].
 //   * Warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warp 2 =
 //     threshold refresh.
+//   * Work units: whole query blocks, or key ranges of a query block split
+//     over several CTAs (they share the query's count and a global histogram).
+//   * ALT form (T <= 4): one query group with a narrower MMA (N = 64 per
+//     query), the two accumulators alternating between tiles, and the unused
+//     query rows used as two more key stages.
 // Every wait is bounded (2 s); on expiry the kernel records LTK_ERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #include <climits>
