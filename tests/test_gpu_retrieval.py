@@ -85,3 +85,27 @@ def test_retrieval_large_k(k):
     S = orc.bf16_to_f64(qb) @ orc.bf16_to_f64(cb).T
     for t in range(0, 48, 5):
         check_row_tolerant(out["idx"][t], out["sc"][t], S[t], k, where=f"query {t}")
+
+
+def test_retrieval_segments_overflow_rescued():
+    """Several corpus ranges per query (one list segment each) with segments far
+    too small: the overflowed queries are recomputed exactly."""
+    qb, cb = _inputs(12, 100003, 256, seed=8, integer=True)
+    out = _run(qb, cb, 300, cand_cap=600)
+    assert out["stats"]["n_overflow"] > 0
+    ref_idx, ref_sc = orc.retrieval_topk(qb, cb, 300)
+    np.testing.assert_array_equal(out["idx"], ref_idx)
+    np.testing.assert_array_equal(out["sc"], ref_sc)
+
+
+def test_retrieval_relu_scores():
+    """One head with ReLU (the retrieval kernel's ReLU form) against the
+    oracle's plain definition with H = 1, w = 1, no mask."""
+    qb, cb = _inputs(33, 20011, 256, seed=9, integer=True)
+    T, d = qb.shape
+    out = _run(qb, cb, 400, relu=1)
+    inp = datagen.IndexerInputs(dtype="bf16", q=qb.reshape(T, 1, d), k=cb,
+                                w=np.ones((T, 1), np.float32), positions=np.zeros(T, np.int32))
+    ref_idx, ref_sc = orc.indexer_topk(inp, 400, causal=False, relu=True)
+    np.testing.assert_array_equal(out["idx"], ref_idx)
+    np.testing.assert_array_equal(out["sc"], ref_sc)

@@ -89,3 +89,21 @@ def test_one_handle_different_cache_lengths():
         idx, sc = _call(op, inp, k)
         check_exact(inp, idx, sc, k)
     op.close()
+
+
+@pytest.mark.parametrize("T,S", [(1, 70000), (3, 40001)])
+def test_small_chunks_fp8(T, S):
+    """e4m3 q/k in the alternating form (its deeper key ring sits in the unused
+    query rows of the e4m3 layout)."""
+    inp = datagen.make_indexer_inputs(T=T, first_pos=S - T, S=S, dtype="fp8", seed=360 + T)
+    op = IndexerTopK(max_T=T, max_S=S, k=1024, dtype="fp8", enable_decoupled=1)
+    idx, sc = _call(op, inp, 1024)
+    import torch
+    d = to_device(inp)
+    di, ds = op.decoupled(d["q"], d["w"], d["k_cache"], d["positions"], k=1024,
+                          q_scale=d["q_scale"], k_scale=d["k_scale"])
+    torch.cuda.synchronize()
+    op.close()
+    np.testing.assert_array_equal(di.cpu().numpy(), idx)
+    np.testing.assert_array_equal(ds.cpu().numpy(), sc)
+    check_tolerant(inp, idx, sc, 1024)
