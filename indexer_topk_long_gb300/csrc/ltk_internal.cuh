@@ -243,19 +243,6 @@ __device__ __forceinline__ void tmem_ld32x16(uint32_t taddr, float (&v)[16]) {
       : "r"(taddr));
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane (shape 32x32b, 32
-// repetitions).  Undefined until tmem_wait_ld_tied on the same array.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
-        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
-        "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]),
-        "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]),
-        "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
-      : "r"(taddr));
-}
 // tcgen05.ld 16x256b, 4 repetitions along columns (32 fp32 columns of 16
 // lanes).  Fragment layout (PTX ISA, tcgen05 matrix fragments, shape
 // 16x256b): in repetition r, thread t holds columns 8r + 2(t%4) + {0,1} of lane
@@ -302,17 +289,6 @@ __device__ __forceinline__ void ffma2_acc(unsigned long long& acc, float a0, flo
   asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(A), "l"(wpair));
 }
-
-// Packed fp32x2 fused multiply-add (sm_100+): acc = a * b + acc, lane-wise.
-__device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
-  unsigned long long A, B, C;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(C) : "f"(acc.x), "f"(acc.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(C) : "l"(A), "l"(B));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(C));
-}
-
 
 // Shared-memory matrix descriptor of a K-major operand stored in the
 // 128-byte-swizzled layout that a TMA load with CU_TENSOR_MAP_SWIZZLE_128B
