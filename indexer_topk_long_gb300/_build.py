@@ -19,7 +19,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libltk.so")
-HEADERS = [os.path.join(CSRC, "ltk_internal.cuh"), os.path.join(ROOT, "include", "ltk.h")]
+HEADERS = [*(os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith(".cuh")),
+           os.path.join(ROOT, "include", "ltk.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                 "--expt-relaxed-constexpr"]

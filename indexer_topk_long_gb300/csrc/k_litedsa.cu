@@ -7,17 +7,16 @@
 //   1. the group's G * k selected indices become 64-bit keys
 //      (index << 8 | query-within-group); invalid slots (-1) and the padding
 //      up to P = E * 1024 keys (E a power of two, 1..16) sort last;
-//   2. a bitonic sort with the keys in registers: thread t holds keys
-//      [t E, t E + E); exchanges at strides below E stay in the thread, strides
-//      up to 32 E go through warp shuffles, and only the longer strides go
-//      through shared memory (stored element-major, so every access is
-//      conflict-free);
+//   2. a bitonic sort with the keys in registers (block_sort.cuh): thread t
+//      holds keys [t E, t E + E); only strides of 32 E and more go through
+//      shared memory;
 //   3. a key starts a run when its index differs from the previous key's; a
 //      block scan of the per-thread run counts gives every key its position j
 //      in the ascending union; the first key of a run writes union[j], and
 //      every key sets bit j of its query's mask (shared-memory atomicOr);
 //   4. lengths, the -1 padding of the union and the masks go to device memory.
 // G * k <= 16384.
+#include "block_sort.cuh"
 #include "ltk_internal.cuh"
 
 namespace ltk {
@@ -25,113 +24,6 @@ namespace {
 
 constexpr int kLdThreads = 1024;
 constexpr int kLdMaxEntries = 16384;
-template <typename K>
-__device__ __forceinline__ K shfl_xor_key(K v, int m) {
-  if constexpr (sizeof(K) == 4) {
-    return __shfl_xor_sync(0xFFFFFFFFu, v, m);
-  } else {
-    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), m);
-    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), m);
-    return (static_cast<K>(hi) << 32) | lo;
-  }
-}
-template <typename K>
-__device__ __forceinline__ K shfl_up_key(K v) {
-  if constexpr (sizeof(K) == 4) {
-    return __shfl_up_sync(0xFFFFFFFFu, v, 1);
-  } else {
-    const uint32_t lo = __shfl_up_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), 1);
-    const uint32_t hi = __shfl_up_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), 1);
-    return (static_cast<K>(hi) << 32) | lo;
-  }
-}
-template <typename K>
-__device__ __forceinline__ K kmin(K a, K b) { return a < b ? a : b; }
-template <typename K>
-__device__ __forceinline__ K kmax(K a, K b) { return a < b ? b : a; }
-
-// In-thread steps of one bitonic merge: pairs (e, e ^ M) with M = size - 1
-// (the mirrored first step, MIRROR) or (e, e + S) (the following steps), both
-// ascending: the lower slot takes the minimum.
-template <int E, int S, bool MIRROR, typename K>
-__device__ __forceinline__ void ld_in_thread(K (&v)[E]) {
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    if ((e & S) == 0) {
-      const int f = MIRROR ? (e ^ (2 * S - 1)) : (e + S);
-      const K a = v[e], b = v[f];
-      v[e] = kmin(a, b);
-      v[f] = kmax(a, b);
-    }
-  }
-}
-
-template <int E, bool MIRROR, typename K>
-__device__ __forceinline__ void ld_in_thread_at(K (&v)[E], int half) {
-  switch (half) {
-    case 1: ld_in_thread<E, 1, MIRROR>(v); break;
-    case 2: if constexpr (E > 2) ld_in_thread<E, 2, MIRROR>(v); break;
-    case 4: if constexpr (E > 4) ld_in_thread<E, 4, MIRROR>(v); break;
-    case 8: if constexpr (E > 8) ld_in_thread<E, 8, MIRROR>(v); break;
-    default: break;
-  }
-}
-
-// Ascending bitonic sort of E * blockDim keys, thread t holding keys
-// [t E, t E + E).  Each merge of blocks of `size` keys starts with the mirrored
-// step (key i against key i ^ (size - 1)) and continues with half strides, so
-// every exchange is ascending and needs no direction: the lower index keeps
-// the minimum.  Strides below E stay in the thread, strides below 32 E use warp
-// shuffles, longer ones the shared-memory buffer xs, stored slot-major
-// (xs[e * blockDim + t]) so that every access is conflict-free.
-template <int E, typename K>
-__device__ void ld_sort(K (&v)[E], K* xs) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int nt = blockDim.x;
-  const int P = E * nt;
-#pragma unroll 1
-  for (int size = 2; size <= P; size <<= 1) {
-#pragma unroll 1
-    for (int half = size >> 1; half > 0; half >>= 1) {
-      const bool mirror = half == (size >> 1);
-      if (half < E) {
-        if constexpr (E > 1) {
-          if (mirror) ld_in_thread_at<E, true>(v, half);
-          else ld_in_thread_at<E, false>(v, half);
-        }
-      } else if (half < 32 * E) {
-        const int lm = mirror ? (size / E - 1) : (half / E);   // partner lane: lane ^ lm
-        const bool lower = (lane & (half / E)) == 0;
-        if (mirror) {
-          K o[E];
-#pragma unroll
-          for (int e = 0; e < E; ++e) o[e] = shfl_xor_key(v[E - 1 - e], lm);   // partner slot E-1-e
-#pragma unroll
-          for (int e = 0; e < E; ++e) v[e] = lower ? kmin(v[e], o[e]) : kmax(v[e], o[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const K o = shfl_xor_key(v[e], lm);
-            v[e] = lower ? kmin(v[e], o) : kmax(v[e], o);
-          }
-        }
-      } else {
-        const int tm = mirror ? (size / E - 1) : (half / E);   // partner thread: tid ^ tm
-        const bool lower = (tid & (half / E)) == 0;
-#pragma unroll
-        for (int e = 0; e < E; ++e) xs[e * nt + tid] = v[e];
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const K o = xs[(mirror ? E - 1 - e : e) * nt + (tid ^ tm)];
-          v[e] = lower ? kmin(v[e], o) : kmax(v[e], o);
-        }
-        __syncthreads();
-      }
-    }
-  }
-}
-
 // Pack one group with keys of type K: index << 8 | query-within-group, none =
 // all ones (sorts last).
 template <int E, typename K>
@@ -154,7 +46,7 @@ __device__ void ld_pack_group(const int* __restrict__ topk, int k, int G, int W,
     }
     v[e] = key;
   }
-  ld_sort<E, K>(v, xs);
+  block_sort_regs<E, false>(v, xs);
 
   // the key before this thread's first key: the previous lane's last, or for
   // lane 0 the previous warp's last

@@ -23,6 +23,7 @@
 #include <climits>
 #include <cmath>
 
+#include "block_sort.cuh"
 #include "ltk_internal.cuh"
 
 namespace ltk {
@@ -236,6 +237,54 @@ __device__ void write_sorted(unsigned long long* buf, int kk, int k, int t, int*
       oi[i] = -1;
       os[i] = -INFINITY;
     }
+  }
+}
+
+// write_sorted for a 1024-thread CTA: the keys go into registers (slot-major
+// loads from buf, conflict-free), a register bitonic sort orders them
+// descending, and thread t writes output slots [t E, t E + E).  buf must hold
+// at least max(next power of two of kk, 1024) keys.  Larger sorts fall back to
+// write_sorted.
+template <int E>
+__device__ void write_sorted_regs(unsigned long long* buf, int kk, int k, int t, int* out_idx,
+                                  float* out_score) {
+  const int nt = blockDim.x, tid = threadIdx.x;
+  const int P = E * nt;
+  for (int i = kk + tid; i < P; i += nt) buf[i] = 0ull;
+  __syncthreads();
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = buf[e * nt + tid];   // any order: the sort follows
+  __syncthreads();
+  block_sort_regs<E, true>(v, buf);
+  int* oi = out_idx + static_cast<size_t>(t) * k;
+  float* os = out_score + static_cast<size_t>(t) * k;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid * E + e;
+    if (i < k) {
+      oi[i] = i < kk ? ckey_idx(v[e]) : -1;
+      os[i] = i < kk ? ckey_score(v[e]) : -INFINITY;
+    }
+  }
+  for (int i = P + tid; i < k; i += nt) {
+    oi[i] = -1;
+    os[i] = -INFINITY;
+  }
+}
+
+__device__ void write_sorted_wide(unsigned long long* buf, int kk, int k, int t, int* out_idx,
+                                  float* out_score) {
+  int P = 1;
+  while (P < kk) P <<= 1;
+  const int nt = blockDim.x;
+  const int E = P <= nt ? 1 : P / nt;
+  switch (E) {
+    case 1: write_sorted_regs<1>(buf, kk, k, t, out_idx, out_score); break;
+    case 2: write_sorted_regs<2>(buf, kk, k, t, out_idx, out_score); break;
+    case 4: write_sorted_regs<4>(buf, kk, k, t, out_idx, out_score); break;
+    case 8: write_sorted_regs<8>(buf, kk, k, t, out_idx, out_score); break;
+    default: write_sorted(buf, kk, k, t, out_idx, out_score); break;
   }
 }
 
@@ -501,7 +550,10 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
   __syncthreads();
   // a large boundary bin was selected unordered: sort the whole output
   if (need_full_sort || (r > 0 && m_bnd > kRankSelect)) {
-    write_sorted(outbuf, kk, p.k, t, p.out_idx, p.out_score);
+    if constexpr (THREADS >= kSelThreadsWide)
+      write_sorted_wide(outbuf, kk, p.k, t, p.out_idx, p.out_score);
+    else
+      write_sorted(outbuf, kk, p.k, t, p.out_idx, p.out_score);
   } else {
     int* oi = p.out_idx + static_cast<size_t>(t) * p.k;
     float* os = p.out_score + static_cast<size_t>(t) * p.k;
@@ -800,6 +852,7 @@ __global__ void __launch_bounds__(kRescueThreads) rescue_kernel(const RescuePara
 size_t outbuf_bytes(int k) {
   int P = 1;
   while (P < k) P <<= 1;
+  if (P < kSelThreadsWide) P = kSelThreadsWide;   // the wide form's sort holds 1024 keys at least
   return static_cast<size_t>(P) * sizeof(unsigned long long);
 }
 
@@ -819,8 +872,10 @@ cudaError_t launch_select_as(const SelectParams& p, int slot, cudaStream_t strea
 cudaError_t launch_select(const SelectParams& p, int num_sms, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
   if (p.seg_cnt != nullptr && (p.nseg < 1 || p.nseg > kMaxSegs)) return cudaErrorInvalidValue;
-  // few queries: one wide CTA each (the per-query work is latency-bound)
-  const bool wide = p.T < num_sms;
+  // one wide CTA per query when there are few queries (the per-query work is
+  // latency-bound) or when k is large (the output buffer then allows one CTA
+  // per SM anyway, and the wide form sorts in registers)
+  const bool wide = p.T < num_sms || p.k > 2048;
   if (p.seg_cnt != nullptr)
     return wide ? launch_select_as<kSelThreadsWide, true>(p, kSlotSelectSegWide, stream)
                 : launch_select_as<kSelThreads, true>(p, kSlotSelectSeg, stream);
