@@ -358,23 +358,33 @@ __global__ void digit_hist_kernel(const unsigned long long* __restrict__ keys, l
     if (h[i]) atomicAdd(&hist[i], h[i]);
 }
 
-__global__ void digit_pick_kernel(unsigned int* hist, int shift, unsigned long long* state) {
-  if (threadIdx.x != 0) return;
+// One CTA of 256 threads: thread t looks at digit 255 - t; a block scan of the
+// counts from the top finds the digit holding the remaining rank, and every
+// thread clears its bin for the next pass.
+__global__ void __launch_bounds__(256) digit_pick_kernel(unsigned int* hist, int shift,
+                                                         unsigned long long* state) {
+  __shared__ long long warp_tot[8];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const long long remaining = static_cast<long long>(state[2]);
-  long long above = 0;
-  int digit = 0;
-  for (int d = 255; d >= 0; --d) {
-    const long long c = hist[d];
-    if (above + c >= remaining) {
-      digit = d;
-      break;
-    }
-    above += c;
+  const int d = 255 - t;
+  const long long c = hist[d];
+  long long incl = c;
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
   }
-  state[0] |= static_cast<uint64_t>(digit) << shift;
-  state[1] |= static_cast<uint64_t>(0xFF) << shift;
-  state[2] = static_cast<uint64_t>(remaining - above);
-  for (int d = 0; d < 256; ++d) hist[d] = 0;
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  for (int i = 0; i < w; ++i) incl += warp_tot[i];
+  const long long above = incl - c;   // keys with a larger digit
+  hist[d] = 0;
+  // (the last digit takes the rank when the counts fall short, as the
+  // sequential scan would)
+  if ((above < remaining && incl >= remaining) || (d == 0 && incl < remaining)) {
+    state[0] |= static_cast<uint64_t>(d) << shift;
+    state[1] |= static_cast<uint64_t>(0xFF) << shift;
+    state[2] = static_cast<uint64_t>(remaining - above);
+  }
 }
 
 __global__ void collect_top_kernel(const unsigned long long* __restrict__ keys, long long S,
@@ -485,7 +495,7 @@ cudaError_t launch_make_sample(const int* prev_idx, long long n_prev, long long 
   init_select_state_kernel<<<1, 256, 0, stream>>>(ws.state, ws.hist, n);
   for (int shift = 56; shift >= 0; shift -= 8) {
     digit_hist_kernel<<<grid_for(S, 256, 1024), 256, 0, stream>>>(ws.keys, S, shift, ws.state, ws.hist);
-    digit_pick_kernel<<<1, 32, 0, stream>>>(ws.hist, shift, ws.state);
+    digit_pick_kernel<<<1, 256, 0, stream>>>(ws.hist, shift, ws.state);
   }
   collect_top_kernel<<<grid_for(S, 256, 4096), 256, 0, stream>>>(ws.keys, S, ws.state, n, out);
   count_launches((n_prev > 0 ? 1 : 0) + 3 + 2 * 8);

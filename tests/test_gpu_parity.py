@@ -153,6 +153,21 @@ def test_make_sample_ranking():
     np.testing.assert_array_equal(np.sort(got[np.isin(got, order)]), np.sort(order[:300]))
 
 
+def test_make_sample_pads_with_unselected_ids():
+    """Fewer selected ids than asked for: all of them, then distinct unselected ones."""
+    import torch
+    S = 3000
+    rng = np.random.default_rng(17)
+    prev = rng.integers(0, S, size=(4, 16)).astype(np.int32)
+    prev[0, :3] = -1
+    op = IndexerTopK(max_T=8, max_S=S, k=64)
+    got = op.make_sample(torch.from_numpy(prev).cuda(), S, 500).cpu().numpy()
+    op.close()
+    chosen = np.unique(prev[prev >= 0])
+    assert len(np.unique(got)) == 500 and got.min() >= 0 and got.max() < S
+    assert np.isin(chosen, got).all()
+
+
 def test_empty_chunk_and_k_larger_than_visible():
     import torch
     inp = datagen.make_indexer_inputs(T=8, first_pos=0, S=700, integer=True, seed=14)
