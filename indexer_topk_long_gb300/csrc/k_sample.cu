@@ -230,6 +230,69 @@ __device__ uint32_t block_select_u32(const uint32_t* vals, int m, int r, unsigne
   return prefix;
 }
 
+constexpr int kStatBins = 1024;
+
+// The r-th largest of m order codes in shared memory (0 = invisible score),
+// the visible scores spanning [lo, hi]: a histogram of kStatBins equal-width
+// bins over [lo, hi] (monotone in the score) finds the bin holding it and the
+// count above that bin; that bin's codes are gathered into hb (the histogram
+// is no longer needed) and a radix select over those few codes finishes.  Two
+// passes over the m codes instead of four; a crowded bin (more than kStatBins
+// codes) falls back to the radix select over all m.
+__device__ uint32_t block_select_binned(const uint32_t* vals, int m, int r, float lo, float hi, unsigned* hb,
+                                        unsigned* hist256, uint32_t* sh_state, unsigned* warp_tot,
+                                        int* sh_int) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int bd = static_cast<int>(blockDim.x);
+  float delta = 0.f;
+  if (hi > lo) {
+    delta = __fdiv_rn(static_cast<float>(kStatBins), __fsub_rn(hi, lo));
+    if (!(delta <= 1e30f)) delta = 1e30f;
+  }
+  for (int i = tid; i < kStatBins; i += bd) hb[i] = 0u;
+  __syncthreads();
+  for (int i = tid; i < m; i += bd) {
+    const uint32_t v = vals[i];
+    if (v != 0u) atomicAdd(&hb[bin_of(unord_f32(v), lo, delta, kStatBins)], 1u);
+  }
+  __syncthreads();
+  // thread t owns bins [top - per, top), top = kStatBins - t * per
+  const int per = kStatBins / bd;
+  const int top = kStatBins - tid * per;
+  int seg = 0;
+  for (int b = top - per; b < top; ++b) seg += static_cast<int>(hb[b]);
+  int incl = seg;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_tot[w] = static_cast<unsigned>(incl);
+  __syncthreads();
+  for (int i = 0; i < w; ++i) incl += static_cast<int>(warp_tot[i]);
+  int above = incl - seg;
+  if (above < r && incl >= r) {
+    int b = top - 1;
+    for (; b > top - per; --b) {
+      if (above + static_cast<int>(hb[b]) >= r) break;
+      above += static_cast<int>(hb[b]);
+    }
+    sh_int[0] = b;
+    sh_int[1] = above;
+    sh_int[2] = static_cast<int>(hb[b]);
+  }
+  if (tid == 0) sh_int[3] = 0;
+  __syncthreads();
+  const int bstar = sh_int[0], cb = sh_int[2];
+  const int r_in = r - sh_int[1];
+  if (cb > kStatBins) return block_select_u32(vals, m, r, hist256, sh_state, warp_tot);
+  for (int i = tid; i < m; i += bd) {
+    const uint32_t v = vals[i];
+    if (v != 0u && bin_of(unord_f32(v), lo, delta, kStatBins) == bstar) hb[atomicAdd(&sh_int[3], 1)] = v;
+  }
+  __syncthreads();
+  return block_select_u32(hb, cb, r_in, hist256, sh_state, warp_tot);
+}
+
 // Per query, from the visible sample scores: the equal-width bins and the
 // start threshold bin.  Bins below the start threshold are never used (the
 // threshold only rises), so the bins span from just below the sample's k-th
@@ -245,7 +308,9 @@ __global__ void __launch_bounds__(THREADS) sample_stats_kernel(const SampleStats
   extern __shared__ uint32_t s_ord[];
   __shared__ unsigned hist256[256];
   __shared__ uint32_t sh_state[2];
-  __shared__ unsigned warp_tot[8];
+  __shared__ unsigned warp_tot[32];
+  __shared__ unsigned hbins[kStatBins];
+  __shared__ int sh_int[4];
   __shared__ float red_min[32], red_max[32];
   __shared__ int red_cnt[32];
   const int t = blockIdx.x;
@@ -292,7 +357,8 @@ __global__ void __launch_bounds__(THREADS) sample_stats_kernel(const SampleStats
   int theta = 0;
   bool ranged = false;
   if (cnt >= p.k && p.k > 0) {
-    const float sk = unord_f32(block_select_u32(s_ord, p.n, p.k, hist256, sh_state, warp_tot));
+    const float sk =
+        unord_f32(block_select_binned(s_ord, p.n, p.k, mn, mx, hbins, hist256, sh_state, warp_tot, sh_int));
     const float span = __fsub_rn(mx, sk);
     if (span > 0.f) {
       const float hi = __fadd_rn(mx, span);
