@@ -236,7 +236,8 @@ constexpr int kStatBins = 1024;
 // the visible scores spanning [lo, hi]: a histogram of kStatBins equal-width
 // bins over [lo, hi] (monotone in the score) finds the bin holding it and the
 // count above that bin; that bin's codes are gathered into hb (the histogram
-// is no longer needed) and a radix select over those few codes finishes.  Two
+// is no longer needed) and ranked by counting, one code per thread (a radix
+// select when the bin holds more codes than the block has threads).  Two
 // passes over the m codes instead of four; a crowded bin (more than kStatBins
 // codes) falls back to the radix select over all m.
 __device__ uint32_t block_select_binned(const uint32_t* vals, int m, int r, float lo, float hi, unsigned* hb,
@@ -290,7 +291,21 @@ __device__ uint32_t block_select_binned(const uint32_t* vals, int m, int r, floa
     if (v != 0u && bin_of(unord_f32(v), lo, delta, kStatBins) == bstar) hb[atomicAdd(&sh_int[3], 1)] = v;
   }
   __syncthreads();
-  return block_select_u32(hb, cb, r_in, hist256, sh_state, warp_tot);
+  if (cb > bd) return block_select_u32(hb, cb, r_in, hist256, sh_state, warp_tot);
+  // rank by counting (one code per thread): code i has rank #{j : c_j > c_i}
+  // + #{j < i : c_j == c_i}, a permutation of 0..cb-1, so exactly one thread
+  // holds rank r_in - 1, and its code is the r_in-th largest
+  if (tid < cb) {
+    const uint32_t v = hb[tid];
+    int rank = 0;
+    for (int j = 0; j < cb; ++j) {
+      const uint32_t u = hb[j];
+      rank += (u > v || (u == v && j < tid)) ? 1 : 0;
+    }
+    if (rank == r_in - 1) sh_state[0] = v;
+  }
+  __syncthreads();
+  return sh_state[0];
 }
 
 // Per query, from the visible sample scores: the equal-width bins and the
@@ -317,6 +332,7 @@ __global__ void __launch_bounds__(THREADS) sample_stats_kernel(const SampleStats
   const float* row = p.scores + static_cast<size_t>(t) * p.ld;
   float mn = INFINITY, mx = -INFINITY;
   int cnt = 0;
+#pragma unroll 4
   for (int i = threadIdx.x; i < p.n; i += blockDim.x) {
     const float v = row[i];
     const bool vis = v != -INFINITY;
@@ -339,15 +355,22 @@ __global__ void __launch_bounds__(THREADS) sample_stats_kernel(const SampleStats
     red_cnt[warp] = cnt;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < static_cast<int>(blockDim.x / 32); ++w) {
-      mn = fminf(mn, red_min[w]);
-      mx = fmaxf(mx, red_max[w]);
-      cnt += red_cnt[w];
+  if (warp == 0) {
+    const bool have = lane < static_cast<int>(blockDim.x / 32);
+    mn = have ? red_min[lane] : INFINITY;
+    mx = have ? red_max[lane] : -INFINITY;
+    cnt = have ? red_cnt[lane] : 0;
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
     }
-    red_min[0] = mn;
-    red_max[0] = mx;
-    red_cnt[0] = cnt;
+    __syncwarp();
+    if (lane == 0) {
+      red_min[0] = mn;
+      red_max[0] = mx;
+      red_cnt[0] = cnt;
+    }
   }
   __syncthreads();
   mn = red_min[0];

@@ -420,7 +420,7 @@ void plan_work(const ltk_handle* h, int T, long long S, bool dense, int* b_full,
     plan_split_cc(T, S, h->num_sms, b_full, s_last);
     *queries_per_unit = 1;
   } else {
-    plan_split(T, S, h->num_sms, dense ? 8 : 32, b_full, s_last);
+    plan_split(T, S, h->num_sms, dense ? 2 : 32, b_full, s_last);
     *queries_per_unit = kTcQPB;
   }
 }

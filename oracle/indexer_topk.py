@@ -171,9 +171,9 @@ def full_scores(inputs, t: int, causal: bool = True, relu: bool = True,
 # ---------------------------------------------------------------------------
 
 
-def retrieval_topk(queries_bits: np.ndarray, corpus_bits: np.ndarray, k: int,
-                   rows=None, block: int = 1 << 18):
-    """Exact top-k inner-product retrieval over a bf16 corpus (fp64 scores).
+def retrieval_scores(queries_bits: np.ndarray, corpus_bits: np.ndarray,
+                     rows=None, block: int = 1 << 18) -> np.ndarray:
+    """fp64 inner products q . c of the chosen queries with every corpus row.
 
     The corpus is widened block by block so that large corpora fit in memory.
     """
@@ -185,8 +185,15 @@ def retrieval_topk(queries_bits: np.ndarray, corpus_bits: np.ndarray, k: int,
     for b0 in range(0, N, block):
         blk = bf16_to_f64(corpus_bits[b0:b0 + block])
         scores[:, b0:b0 + blk.shape[0]] = qsel @ blk.T
-    out_idx = np.full((len(qsel), k), -1, dtype=np.int32)
-    out_val = np.full((len(qsel), k), -np.inf, dtype=np.float32)
-    for r in range(qsel.shape[0]):
+    return scores
+
+
+def retrieval_topk(queries_bits: np.ndarray, corpus_bits: np.ndarray, k: int,
+                   rows=None, block: int = 1 << 18):
+    """Exact top-k inner-product retrieval over a bf16 corpus (fp64 scores)."""
+    scores = retrieval_scores(queries_bits, corpus_bits, rows=rows, block=block)
+    out_idx = np.full((scores.shape[0], k), -1, dtype=np.int32)
+    out_val = np.full((scores.shape[0], k), -np.inf, dtype=np.float32)
+    for r in range(scores.shape[0]):
         out_idx[r], out_val[r] = exact_topk_row(scores[r], k)
     return out_idx, out_val

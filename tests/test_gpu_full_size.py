@@ -7,14 +7,16 @@ chunk); every query is checked for the invariants that hold at any size
 (sorted output, distinct indices, no index beyond the query's position,
 exactly min(k, V) valid entries), and at 128K and 1M the same-GPU decoupled
 baseline -- a second, independent selection path over the same fp32 scores --
-must return identical results for all queries.
+must return identical results for all queries.  The vector-retrieval workload
+runs at its full size too (sampled queries against the oracle's fp64 scores
+over the whole corpus, every query against the decoupled path).
 """
 import numpy as np
 import pytest
 
 import oracle.indexer_topk as orc
 from indexer_topk_long_gb300 import IndexerTopK, datagen
-from parity import check_tolerant, to_device
+from parity import check_row_tolerant, check_tolerant, to_device
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -106,3 +108,37 @@ def test_1m_chunk_bf16():
 def test_1m_chunk_fp8():
     out = _chunk_pair("1m_prev", "1m", "fp8", 8, decoupled=False)
     assert out["stats"]["n_overflow"] == 0
+
+
+def test_retrieval_full_size():
+    """Vector retrieval at the full workload size: 1024 queries x 8,388,608
+    corpus rows, d = 768, k = 1000, sample 3000 -- the configuration bench.py
+    times.  Sampled queries against the oracle's fp64 scores over the whole
+    corpus; every query against the same-GPU decoupled path (same fp32 scores,
+    independent selection) and the invariants."""
+    import torch
+    T, N, d, k = 1024, 8388608, 768, 1000
+    q, c = datagen.retrieval_inputs_torch(N, T, d, seed=20260715, device="cuda")
+    op = IndexerTopK(max_T=T, max_S=N, k=k, heads=1, dim=d, sample_size=3000, enable_decoupled=1)
+    qi, ci = q.view(torch.int16), c.view(torch.int16)
+    w = torch.ones((T, 1), dtype=torch.float32, device="cuda")
+    idx, sc = op(qi, w, ci, None, k=k)
+    torch.cuda.synchronize()
+    st = op.stats()
+    assert st["device_status"] == 0 and st["visible_pairs"] == T * N
+    d_idx, d_sc = op.decoupled(qi, w, ci, None, k=k)
+    torch.cuda.synchronize()
+    if st["n_overflow"] == 0:
+        assert torch.equal(d_idx, idx) and torch.equal(d_sc, sc)
+    op.close()
+    del d_idx, d_sc
+    idx_h, sc_h = idx.cpu().numpy(), sc.cpu().numpy()
+    _invariants(idx_h, sc_h, np.full(T, N - 1, np.int32), N, k)
+    qb = qi.cpu().numpy().view(np.uint16)
+    cb = ci.cpu().numpy().view(np.uint16)
+    del q, c, qi, ci, idx, sc
+    torch.cuda.empty_cache()
+    rows = _sample_queries(T, 4, 9)
+    I = orc.retrieval_scores(qb, cb, rows=rows)
+    for r, t in enumerate(rows):
+        check_row_tolerant(idx_h[t], sc_h[t], I[r], k, where=f"query {t}")
