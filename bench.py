@@ -27,6 +27,7 @@ import signal
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -134,7 +135,9 @@ def recorded_traffic(profile: str, sources=None):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms.  The raw
+    samples go to clocks_<pid>.csv in $LTK_CLOCKS_DIR (default: the system
+    temporary directory)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -143,7 +146,8 @@ class ClockSampler:
     def __init__(self, uuid: str | None):
         self.proc = None
         self.uuid = uuid
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(os.environ.get("LTK_CLOCKS_DIR") or tempfile.gettempdir(),
+                                 f"clocks_{os.getpid()}.csv")
 
     def start(self):
         try:

@@ -85,7 +85,7 @@ def load_library() -> ctypes.CDLL:
         return _LIB
     path = library_path()
     if not os.path.exists(path):
-        raise LtkError(2, f"{path} is not built (run __graft_entry__.build())")
+        raise LtkError(2, f"{path} is not built (python -m indexer_topk_long_gb300._build)")
     lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGS.items():
         fn = getattr(lib, name)
