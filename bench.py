@@ -394,8 +394,8 @@ def run_retrieval(args):
                        "d2h_bytes_per_step": T * R["k"] * 8, "ms_per_step": e_ms / args.steps}
     if not args.no_cpu and world == 1 and rank == 0:
         import oracle.indexer_topk as orc
-        n_rows = 1 << 20
-        sel = [0, T // 2, T - 1]
+        n_rows = R["N"]   # the whole corpus (~10 s of widening and products on the host)
+        sel = sorted({0, T // 3, (2 * T) // 3, T - 1})
         qh = qi[sel].cpu().numpy().view(np.uint16)
         ch = ci[:n_rows].cpu().numpy().view(np.uint16)
         t0 = time.perf_counter()
