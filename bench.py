@@ -94,6 +94,27 @@ def whole_job_value(pairs_per_step: int, steps: int, world: int, elapsed_ms: flo
     return world * pairs_per_step * steps / (elapsed_ms * 1e-3)
 
 
+def host_cpu() -> str:
+    """CPU model of this host (lscpu, else /proc/cpuinfo, else the machine
+    type), reported beside the CPU baseline's core count."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -275,7 +296,7 @@ def run_reference(args):
         "data": "synthetic (seeded hot-key/topic generator)",
         "config": {"workload": f"{args.workload} chunk, {args.dtype} inputs widened to fp64, k={wl.k}",
                    "sample": f"{args.ref_queries} random queries of the chunk per step"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cpu": host_cpu(), "kind": "oracle",
                          "sample": f"{args.ref_queries} queries per step x {args.steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -402,8 +423,9 @@ def run_retrieval(args):
         orc.retrieval_topk(qh, ch, R["k"])
         secs = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": len(sel) * n_rows / secs, "unit": UNIT, "cores": os.cpu_count(),
+                                "cpu": host_cpu(),
                                 "kind": "oracle", "seconds": secs,
-                                "sample": f"{len(sel)} queries against the first {n_rows} corpus rows"}
+                                "sample": f"{len(sel)} queries against the whole corpus ({n_rows} rows)"}
     op.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -709,7 +731,7 @@ def main():
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     if not args.no_cpu and world == 1 and rank == 0:
         rate, secs, desc = cpu_oracle_rate(inp, k, args.cpu_queries)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(), "cpu": host_cpu(),
                                 "kind": "oracle", "sample": desc, "seconds": secs}
 
     op.close()
