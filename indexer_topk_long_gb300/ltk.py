@@ -120,6 +120,70 @@ def _stream_handle(stream) -> int | None:
     return s.cuda_stream
 
 
+def _tensor_ok(t, name: str, numel: int, elem_size: int, device_type: str,
+               dtype=None, device_index=None) -> None:
+    """One tensor argument: device, contiguity, element size (and type) and
+    element count, so that the kernels behind the plain pointers of the C ABI
+    never read or write past the tensor's end."""
+    if t.device.type != device_type:
+        raise ValueError(f"{name}: expected a {device_type} tensor, got one on {t.device}")
+    if device_index is not None and t.device.index != device_index:
+        raise ValueError(f"{name}: on {t.device}, but the current device is cuda:{device_index}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.element_size() != elem_size or (dtype is not None and t.dtype != dtype):
+        want = str(dtype).replace("torch.", "") if dtype is not None else f"{elem_size}-byte"
+        raise ValueError(f"{name}: expected {want} elements, got {t.dtype}")
+    if t.numel() != numel:
+        raise ValueError(f"{name}: expected {numel} elements, got {t.numel()} (shape {tuple(t.shape)})")
+
+
+def check_inputs(heads: int, dim: int, dtype: str, causal: bool, q, w, k_cache, positions=None,
+                 q_scale=None, k_scale=None, prev_topk=None, out=None, k: int | None = None,
+                 device_type: str = "cuda", device_index=None) -> tuple[int, int]:
+    """Validates the tensors of one indexer call before anything is enqueued.
+
+    T = q.shape[0] queries and S = k_cache.shape[0] keys; q holds T * heads *
+    dim codes (2-byte bf16 or 1-byte e4m3), k_cache S * dim codes, w T * heads
+    fp32 weights, positions T int32 (required by a causal handle), q_scale T
+    and k_scale S fp32 (e4m3), prev_topk int32 key ids, out (int32, fp32) with
+    T * k elements each.  Every tensor must be contiguous and on
+    ``device_type``.  Raises ValueError; returns (T, S)."""
+    import torch
+    T, S = int(q.shape[0]), int(k_cache.shape[0])
+    code = 2 if dtype == "bf16" else 1
+    dev = dict(device_type=device_type, device_index=device_index)
+    _tensor_ok(q, "q", T * heads * dim, code, **dev)
+    _tensor_ok(k_cache, "k_cache", S * dim, code, **dev)
+    _tensor_ok(w, "w", T * heads, 4, dtype=torch.float32, **dev)
+    if positions is not None:
+        _tensor_ok(positions, "positions", T, 4, dtype=torch.int32, **dev)
+    elif causal and T > 0:
+        raise ValueError("positions: required by a causal handle")
+    if dtype == "fp8":
+        for t, name, n in ((q_scale, "q_scale", T), (k_scale, "k_scale", S)):
+            if t is not None:
+                _tensor_ok(t, name, n, 4, dtype=torch.float32, **dev)
+            elif T > 0:
+                raise ValueError(f"{name}: required for e4m3 inputs")
+    if prev_topk is not None:
+        _tensor_ok(prev_topk, "prev_topk", prev_topk.numel(), 4, dtype=torch.int32, **dev)
+    if out is not None:
+        n = T * int(k)
+        _tensor_ok(out[0], "out[0] (indices)", n, 4, dtype=torch.int32, **dev)
+        _tensor_ok(out[1], "out[1] (scores)", n, 4, dtype=torch.float32, **dev)
+    return T, S
+
+
+def _index_matrix_ok(t, name: str) -> None:
+    """A [rows, cols] int32 CUDA tensor of key indices on the current device."""
+    import torch
+    if t.dim() != 2:
+        raise ValueError(f"{name}: expected a 2-D [rows, k] tensor, got shape {tuple(t.shape)}")
+    _tensor_ok(t, name, t.numel(), 4, "cuda", dtype=torch.int32,
+               device_index=torch.cuda.current_device())
+
+
 def config_defaults(heads=64, dim=128, k=2048, max_T=8192, max_S=1 << 20) -> Config:
     lib = load_library()
     cfg = Config()
@@ -141,6 +205,7 @@ def litedsa_pack(topk_idx, group: int, stream=None):
     masks [T, ceil(group*k/32)] int32 holding the uint32 bit patterns)."""
     import torch
     lib = load_library()
+    _index_matrix_ok(topk_idx, "topk_idx")
     T, k = int(topk_idx.shape[0]), int(topk_idx.shape[1])
     n_groups = (T + group - 1) // group
     words = (group * k + 31) // 32
@@ -172,12 +237,12 @@ class IndexerTopK:
         self.dtype = dtype
 
     # -- helpers ---------------------------------------------------------
-    def _elem_ok(self, t, name):
+    def _check(self, device_type, q, w, k_cache, positions, q_scale, k_scale, prev_topk, out, k):
         import torch
-        want = 2 if self.dtype == "bf16" else 1
-        if t.element_size() != want or not t.is_contiguous() or t.device.type != "cuda":
-            raise ValueError(f"{name}: need a contiguous CUDA tensor of {want}-byte elements")
-        del torch
+        idx = torch.cuda.current_device() if device_type == "cuda" else None
+        return check_inputs(self.cfg.heads, self.cfg.dim, self.dtype, bool(self.cfg.causal), q, w,
+                            k_cache, positions, q_scale, k_scale, prev_topk, out, k,
+                            device_type=device_type, device_index=idx)
 
     def _outputs(self, T, k, device, out):
         import torch
@@ -190,10 +255,8 @@ class IndexerTopK:
     def topk(self, q, w, k_cache, positions=None, k: int | None = None, prev_topk=None,
              q_scale=None, k_scale=None, out=None, stream=None):
         """Fused exact top-k; returns (idx int32 [T,k], score fp32 [T,k])."""
-        T, S = int(q.shape[0]), int(k_cache.shape[0])
         k = int(k or self.cfg.k)
-        self._elem_ok(q, "q")
-        self._elem_ok(k_cache, "k_cache")
+        T, S = self._check("cuda", q, w, k_cache, positions, q_scale, k_scale, prev_topk, out, k)
         oi, os_ = self._outputs(T, k, q.device, out)
         n_prev = 0 if prev_topk is None else int(prev_topk.numel())
         _check(self.lib.ltk_indexer_topk(self.h, _ptr(q), _ptr(q_scale), _ptr(w), _ptr(k_cache),
@@ -208,8 +271,8 @@ class IndexerTopK:
                   q_scale=None, k_scale=None, out=None, stream=None):
         """Same as topk, but all tensors live in (pinned) host memory."""
         import torch
-        T, S = int(q.shape[0]), int(k_cache.shape[0])
         k = int(k or self.cfg.k)
+        T, S = self._check("cpu", q, w, k_cache, positions, q_scale, k_scale, prev_topk, out, k)
         if out is None:
             out = (torch.empty((T, k), dtype=torch.int32, pin_memory=True),
                    torch.empty((T, k), dtype=torch.float32, pin_memory=True))
@@ -224,10 +287,8 @@ class IndexerTopK:
     def decoupled(self, q, w, k_cache, positions=None, k: int | None = None, q_scale=None,
                   k_scale=None, out=None, stream=None):
         """Decoupled baseline: materialised scores + row radix select."""
-        T, S = int(q.shape[0]), int(k_cache.shape[0])
         k = int(k or self.cfg.k)
-        self._elem_ok(q, "q")
-        self._elem_ok(k_cache, "k_cache")
+        T, S = self._check("cuda", q, w, k_cache, positions, q_scale, k_scale, None, out, k)
         oi, os_ = self._outputs(T, k, q.device, out)
         _check(self.lib.ltk_decoupled_topk(self.h, _ptr(q), _ptr(q_scale), _ptr(w), _ptr(k_cache),
                                            _ptr(k_scale), _ptr(positions), T, S, k, _ptr(oi),
@@ -245,6 +306,8 @@ class IndexerTopK:
     def make_sample(self, prev_idx, S: int, n: int | None = None, stream=None):
         import torch
         n = int(n or min(3 * self.cfg.k, 16384))
+        if prev_idx is not None:
+            _index_matrix_ok(prev_idx, "prev_idx")
         out = torch.empty(n, dtype=torch.int32, device="cuda")
         T_prev, k_prev = (int(prev_idx.shape[0]), int(prev_idx.shape[1])) if prev_idx is not None else (0, 0)
         _check(self.lib.ltk_make_sample(self.h, _ptr(prev_idx), T_prev, k_prev, S, n, _ptr(out),
