@@ -65,18 +65,34 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     return np.where((c & 0x7F) == 0x7F, np.nan, out)
 
 
-def widen(inputs) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
-    """(q [T,H,d], w [T,H], k [S,d]) in float64 from an input bundle.
+def widen_queries(inputs) -> tuple[np.ndarray, np.ndarray]:
+    """(q [T,H,d], w [T,H]) in float64 from an input bundle.
 
-    fp8: q = code(q) * q_scale[t], k = code(k) * k_scale[s]  (per-token scales).
+    bf16: q is the widened bf16 value.  fp8 e4m3 with per-token scales: the
+    value of query t is code(q[t,h,i]) * q_scale[t] -- one fp32 scale per
+    query token, shared by all its heads and dimensions.  w is fp32 in both
+    formats and is never scaled.
     """
     w = np.asarray(inputs.w, dtype=np.float32).astype(np.float64)
     if inputs.dtype == "bf16":
-        return bf16_to_f64(inputs.q), w, bf16_to_f64(inputs.k)
+        return bf16_to_f64(inputs.q), w
     if inputs.dtype == "fp8":
-        q = e4m3_to_f64(inputs.q) * np.asarray(inputs.q_scale, np.float32).astype(np.float64)[:, None, None]
-        k = e4m3_to_f64(inputs.k) * np.asarray(inputs.k_scale, np.float32).astype(np.float64)[:, None]
-        return q, w, k
+        qs = np.asarray(inputs.q_scale, np.float32).astype(np.float64)
+        return e4m3_to_f64(inputs.q) * qs[:, None, None], w
+    raise ValueError(inputs.dtype)
+
+
+def widen_keys(inputs) -> np.ndarray:
+    """k [S,d] in float64 from an input bundle.
+
+    bf16: the widened bf16 value.  fp8 e4m3: code(k[s,i]) * k_scale[s], one
+    fp32 scale per key token.
+    """
+    if inputs.dtype == "bf16":
+        return bf16_to_f64(inputs.k)
+    if inputs.dtype == "fp8":
+        ks = np.asarray(inputs.k_scale, np.float32).astype(np.float64)
+        return e4m3_to_f64(inputs.k) * ks[:, None]
     raise ValueError(inputs.dtype)
 
 
@@ -126,7 +142,7 @@ def indexer_topk(inputs, k: int, causal: bool = True, relu: bool = True,
     Returns (idx int32 [n, k], score fp32 [n, k]).  ``keys64`` may pass the
     already-widened key matrix to avoid re-widening it for large contexts.
     """
-    q, w, _ = widen_queries_only(inputs)
+    q, w = widen_queries(inputs)
     kk = widen_keys(inputs) if keys64 is None else keys64
     T = q.shape[0]
     S = kk.shape[0]
@@ -142,25 +158,10 @@ def indexer_topk(inputs, k: int, causal: bool = True, relu: bool = True,
     return out_idx, out_val
 
 
-def widen_queries_only(inputs):
-    """(q, w, None): widen only the query side (keys passed separately)."""
-    w = np.asarray(inputs.w, dtype=np.float32).astype(np.float64)
-    if inputs.dtype == "bf16":
-        return bf16_to_f64(inputs.q), w, None
-    q = e4m3_to_f64(inputs.q) * np.asarray(inputs.q_scale, np.float32).astype(np.float64)[:, None, None]
-    return q, w, None
-
-
-def widen_keys(inputs) -> np.ndarray:
-    if inputs.dtype == "bf16":
-        return bf16_to_f64(inputs.k)
-    return e4m3_to_f64(inputs.k) * np.asarray(inputs.k_scale, np.float32).astype(np.float64)[:, None]
-
-
 def full_scores(inputs, t: int, causal: bool = True, relu: bool = True,
                 keys64: np.ndarray | None = None) -> np.ndarray:
     """All visible scores of query t in fp64 (used by tolerance checks)."""
-    q, w, _ = widen_queries_only(inputs)
+    q, w = widen_queries(inputs)
     kk = widen_keys(inputs) if keys64 is None else keys64
     V = visible_count(inputs.positions[t], kk.shape[0], causal)
     return scores_one_query(q[t], w[t], kk[:V], relu)

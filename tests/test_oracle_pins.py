@@ -31,6 +31,23 @@ class _Bundle:
         self.positions = np.asarray(positions, np.int32)
 
 
+class _Fp8Bundle:
+    """Input bundle of e4m3 codes with fp32 per-token scales."""
+
+    def __init__(self, q_codes, q_scale, w, k_codes, k_scale, positions):
+        self.dtype = "fp8"
+        self.q = np.asarray(q_codes, np.uint8)
+        self.k = np.asarray(k_codes, np.uint8)
+        self.q_scale = np.asarray(q_scale, np.float32)
+        self.k_scale = np.asarray(k_scale, np.float32)
+        self.w = np.asarray(w, np.float32)
+        self.positions = np.asarray(positions, np.int32)
+
+
+def _hex(a):
+    return np.vectorize(lambda c: int(c, 16))(np.asarray(a, dtype=object)).astype(np.uint8)
+
+
 def _f(x):
     return -math.inf if x == "-inf" else float(x)
 
@@ -151,23 +168,85 @@ def pin_fp_formats():
 
 
 def pin_fp8_bundle_is_scaled_product():
-    """fp8 bundle: the widened value is code value times the per-token scale."""
-    rng = np.random.default_rng(9)
-    codes = np.array([[0x38, 0x40, 0xB8, 0x01]], np.uint8)   # 1, 2, -1, 2^-9
-    scale = np.array([0.25], np.float32)
-
-    class B:
-        dtype = "fp8"
-        q = codes.reshape(1, 1, 4)
-        k = codes
-        q_scale = scale
-        k_scale = np.array([4.0], np.float32)
-        w = np.ones((1, 1), np.float32)
-        positions = np.zeros(1, np.int32)
-    q, w, k = orc.widen(B)
+    """fp8 bundle: the widened value is code value times its own token's scale."""
+    codes = np.array([[0x38, 0x40, 0xB8, 0x01], [0x38, 0x40, 0xB8, 0x01]], np.uint8)   # 1, 2, -1, 2^-9
+    b = _Fp8Bundle(codes.reshape(2, 1, 4), [0.25, 8.0], np.ones((2, 1)), codes, [4.0, 0.5], [1, 1])
+    q, w = orc.widen_queries(b)
+    k = orc.widen_keys(b)
     np.testing.assert_array_equal(q[0, 0], [0.25, 0.5, -0.25, 0.25 * 2 ** -9])
+    np.testing.assert_array_equal(q[1, 0], [8.0, 16.0, -8.0, 8 * 2 ** -9])
     np.testing.assert_array_equal(k[0], [4.0, 8.0, -4.0, 4 * 2 ** -9])
-    del rng
+    np.testing.assert_array_equal(k[1], [0.5, 1.0, -0.5, 0.5 * 2 ** -9])
+    np.testing.assert_array_equal(w, np.ones((2, 1)))
+
+
+def pin_fp8_hand_examples():
+    """Hand-derived e4m3 indexer case with per-token scales (tests/golden)."""
+    with open(os.path.join(GOLDEN, "hand_examples.json")) as f:
+        cases = json.load(f)["fp8_cases"]
+    for case in cases:
+        qc, kc = _hex(case["q_codes"]), _hex(case["k_codes"])
+        for run in case["runs"]:
+            b = _Fp8Bundle(qc, case["q_scale"], case["w"], kc, case["k_scale"], run["positions"])
+            idx, val = orc.indexer_topk(b, case["k"])
+            np.testing.assert_array_equal(idx, np.array(run["idx"], np.int32), err_msg=case["name"])
+            np.testing.assert_array_equal(val, np.array(run["score"], np.float32), err_msg=case["name"])
+        b = _Fp8Bundle(qc, case["q_scale"], case["w"], kc, case["k_scale"], [len(kc) - 1] * len(qc))
+        for t, row in enumerate(case["all_scores"]):
+            np.testing.assert_array_equal(orc.full_scores(b, t), row)
+
+
+def _fp8_random_bundle(rng, T, H, d, S, pow2_scales=True):
+    qv = rng.standard_normal((T, H, d)) * 4
+    kv = rng.standard_normal((S, d)) * 4
+    qc, kc = datagen.e4m3_codes(qv), datagen.e4m3_codes(kv)
+    if pow2_scales:
+        qs = np.exp2(rng.integers(-3, 4, size=T)).astype(np.float32)
+        ks = np.exp2(rng.integers(-3, 4, size=S)).astype(np.float32)
+    else:
+        qs = np.ones(T, np.float32)
+        ks = np.ones(S, np.float32)
+    w = (rng.standard_normal((T, H)) / 4).astype(np.float32)   # either sign
+    return _Fp8Bundle(qc, qs, w, kc, ks, np.full(T, S - 1))
+
+
+def pin_fp8_scale_homogeneity():
+    """ReLU(a x) = a ReLU(x) for a > 0, so the score with per-token scales is
+    q_scale[t] * k_scale[s] times the score of the bare codes.  Power-of-two
+    scales keep both sides exact."""
+    rng = np.random.default_rng(10)
+    T, H, d, S = 3, 4, 8, 20
+    b = _fp8_random_bundle(rng, T, H, d, S)
+    bare = _Fp8Bundle(b.q, np.ones(T), b.w, b.k, np.ones(S), b.positions)
+    for t in range(T):
+        expect = orc.full_scores(bare, t) * float(b.q_scale[t]) * b.k_scale.astype(np.float64)
+        np.testing.assert_array_equal(orc.full_scores(b, t), expect)
+
+
+def pin_fp8_matches_bf16_of_same_values():
+    """An e4m3 code times a power-of-two scale is exactly a bf16 value (3 vs 7
+    mantissa bits): the fp8 bundle and the bf16 bundle of the same real
+    numbers (codes decoded by torch's float8_e4m3fn, not by the oracle) must
+    give identical top-k results."""
+    rng = np.random.default_rng(11)
+    T, H, d, S, k = 4, 3, 8, 40, 7
+    b = _fp8_random_bundle(rng, T, H, d, S)
+    b.positions = np.array([5, 17, 30, 39], np.int32)
+    qv = _e4m3_by_torch(b.q) * b.q_scale[:, None, None].astype(np.float64)
+    kv = _e4m3_by_torch(b.k) * b.k_scale[:, None].astype(np.float64)
+    bf = _Bundle(qv.astype(np.float32), b.w, kv.astype(np.float32), b.positions)
+    assert np.array_equal(orc.bf16_to_f64(bf.q), qv) and np.array_equal(orc.bf16_to_f64(bf.k), kv)
+    i8, v8 = orc.indexer_topk(b, k)
+    i16, v16 = orc.indexer_topk(bf, k)
+    np.testing.assert_array_equal(i8, i16)
+    np.testing.assert_array_equal(v8, v16)
+
+
+def _e4m3_by_torch(codes):
+    """e4m3 values decoded by a different library (torch.float8_e4m3fn)."""
+    torch = pytest.importorskip("torch")
+    c = torch.from_numpy(np.ascontiguousarray(codes, np.uint8))
+    return c.view(torch.float8_e4m3fn).double().numpy()
 
 
 def pin_invariants_gaussian():
@@ -188,6 +267,7 @@ def pin_invariants_gaussian():
 
 PINS = [pin_hand_examples, pin_basis_keys, pin_identical_heads_closed_form, pin_bruteforce_subsets,
         pin_retrieval_vs_torch_topk, pin_fp_formats, pin_fp8_bundle_is_scaled_product,
+        pin_fp8_hand_examples, pin_fp8_scale_homogeneity, pin_fp8_matches_bf16_of_same_values,
         pin_invariants_gaussian]
 
 
@@ -247,8 +327,52 @@ def _mut_ascending(scores, k):
 
 
 def _mut_w_transposed(inputs):
-    q, w, _ = ORIG["widen_queries_only"](inputs)
-    return q, (w.T if w.shape[0] == w.shape[1] else w[::-1]), None
+    q, w = ORIG["widen_queries"](inputs)
+    return q, (w.T if w.shape[0] == w.shape[1] else w[::-1])
+
+
+def _q_codes(inputs):
+    return ORIG["e4m3_to_f64"](inputs.q)
+
+
+def _mut_q_scale_dropped(inputs):
+    if inputs.dtype != "fp8":
+        return ORIG["widen_queries"](inputs)
+    return _q_codes(inputs), np.asarray(inputs.w, np.float64)
+
+
+def _mut_k_scale_dropped(inputs):
+    if inputs.dtype != "fp8":
+        return ORIG["widen_keys"](inputs)
+    return ORIG["e4m3_to_f64"](inputs.k)
+
+
+def _mut_q_scale_on_head_axis(inputs):
+    if inputs.dtype != "fp8":
+        return ORIG["widen_queries"](inputs)
+    qs = np.asarray(inputs.q_scale, np.float64)
+    return _q_codes(inputs) * qs[None, :, None], np.asarray(inputs.w, np.float64)
+
+
+def _mut_q_scale_of_wrong_query(inputs):
+    if inputs.dtype != "fp8":
+        return ORIG["widen_queries"](inputs)
+    qs = np.asarray(inputs.q_scale, np.float64)[::-1]
+    return _q_codes(inputs) * qs[:, None, None], np.asarray(inputs.w, np.float64)
+
+
+def _mut_k_scale_of_wrong_key(inputs):
+    if inputs.dtype != "fp8":
+        return ORIG["widen_keys"](inputs)
+    ks = np.asarray(inputs.k_scale, np.float64)[::-1]
+    return ORIG["e4m3_to_f64"](inputs.k) * ks[:, None]
+
+
+def _mut_w_scaled_twice(inputs):
+    q, w = ORIG["widen_queries"](inputs)
+    if inputs.dtype != "fp8":
+        return q, w
+    return q, w * np.asarray(inputs.q_scale, np.float64)[:, None]
 
 
 def _mut_e4m3_bias8(codes):
@@ -261,7 +385,7 @@ def _mut_bf16_shift(bits):
 
 
 ORIG = {name: getattr(orc, name) for name in
-        ["scores_one_query", "visible_count", "exact_topk_row", "widen_queries_only",
+        ["scores_one_query", "visible_count", "exact_topk_row", "widen_queries", "widen_keys",
          "e4m3_to_f64", "bf16_to_f64"]}
 
 MUTANTS = [
@@ -273,7 +397,13 @@ MUTANTS = [
     ("visible_count", _mut_drop_last_key),
     ("exact_topk_row", _mut_ties_high_index),
     ("exact_topk_row", _mut_ascending),
-    ("widen_queries_only", _mut_w_transposed),
+    ("widen_queries", _mut_w_transposed),
+    ("widen_queries", _mut_q_scale_dropped),
+    ("widen_keys", _mut_k_scale_dropped),
+    ("widen_queries", _mut_q_scale_on_head_axis),
+    ("widen_queries", _mut_q_scale_of_wrong_query),
+    ("widen_keys", _mut_k_scale_of_wrong_key),
+    ("widen_queries", _mut_w_scaled_twice),
     ("e4m3_to_f64", _mut_e4m3_bias8),
     ("bf16_to_f64", _mut_bf16_shift),
 ]
