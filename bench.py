@@ -70,6 +70,12 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decoupled", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="1M bf16 run only: skip the e4m3, 256K and decode sub-records")
+    ap.add_argument("--cpu-single-queries", type=int, default=16,
+                    help="queries of the chunk the single-threaded CPU oracle baseline scores")
+    ap.add_argument("--oracle-child", default="",
+                    help=argparse.SUPPRESS)   # internal: time the oracle on a saved sample
     return ap.parse_args()
 
 
@@ -246,21 +252,75 @@ def to_dev(inp, torch, dev):
                 positions=torch.from_numpy(inp.positions).to(dev), q_scale=qs, k_scale=ks)
 
 
-def cpu_oracle_rate(inp, k: int, n_queries: int):
-    """Oracle (plain fp64 definition + full sort) on a bounded sample of the
-    chunk's queries; returns (pairs/s, seconds, sample description)."""
+def _sample_queries(T: int, n: int) -> list[int]:
+    """n queries evenly spaced over the chunk, first and last included."""
+    import numpy as np
+    return sorted(set(np.linspace(0, T - 1, max(n, 1)).astype(int).tolist()))
+
+
+def oracle_child(path: str) -> int:
+    """Child process of the CPU baseline: load a saved sample of the chunk, time
+    the oracle on it with the BLAS/OpenMP thread count its environment sets,
+    print one JSON line {seconds, pairs}."""
     import numpy as np
     import oracle.indexer_topk as orc
-    keys64 = orc.widen_keys(inp)
-    T = inp.T
-    sel = sorted(set(np.linspace(0, T - 1, max(n_queries, 1)).astype(int).tolist()))
-    pairs = sum(orc.visible_count(inp.positions[t], inp.S, True) for t in sel)
+    z = np.load(path)
+
+    class Chunk:   # the fields the oracle reads
+        dtype = str(z["dtype"])
+        q, w, k, positions = z["q"], z["w"], z["k"], z["positions"]
+        q_scale = z["q_scale"] if "q_scale" in z else None
+        k_scale = z["k_scale"] if "k_scale" in z else None
+    keys64 = orc.widen_keys(Chunk)
+    sel = list(range(Chunk.q.shape[0]))
+    pairs = sum(orc.visible_count(Chunk.positions[t], keys64.shape[0], True) for t in sel)
     t0 = time.perf_counter()
-    orc.indexer_topk(inp, k, queries=sel, keys64=keys64)
-    dt = time.perf_counter() - t0
-    return pairs / dt, dt, (f"{len(sel)} of {T} queries evenly spaced over the chunk "
+    orc.indexer_topk(Chunk, int(z["k_top"]), queries=sel, keys64=keys64)
+    print(json.dumps({"seconds": time.perf_counter() - t0, "pairs": int(pairs)}), flush=True)
+    return 0
+
+
+def cpu_oracle_rate(inp, k: int, n_queries: int, threads: int):
+    """Oracle (plain fp64 definition + full sort) on a bounded sample of the
+    chunk's queries, in a child process whose BLAS/OpenMP pools hold
+    ``threads`` threads; returns (pairs/s, seconds, sample description)."""
+    import numpy as np
+    sel = _sample_queries(inp.T, n_queries)
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    try:
+        extra = {}
+        if inp.dtype == "fp8":
+            extra = {"q_scale": inp.q_scale[sel], "k_scale": inp.k_scale}
+        np.savez(path, dtype=np.array(inp.dtype), q=inp.q[sel], w=inp.w[sel], k=inp.k,
+                 positions=inp.positions[sel], k_top=np.array(k), **extra)
+        env = dict(os.environ)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                    "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS"):
+            env[var] = str(threads)
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", path],
+                             env=env, capture_output=True, text=True, timeout=900, check=True)
+        res = json.loads(out.stdout.strip().splitlines()[-1])
+    finally:
+        os.unlink(path)
+    dt, pairs = res["seconds"], res["pairs"]
+    return pairs / dt, dt, (f"{len(sel)} of {inp.T} queries evenly spaced over the chunk "
                             f"(first and last included), {pairs} visible pairs; key cache "
                             f"widened to fp64 once before timing")
+
+
+def cpu_baseline_record(inp, k: int, n_single: int, n_all: int) -> dict:
+    """The oracle timed single-threaded (the baseline) and on all host cores."""
+    cores = os.cpu_count() or 1
+    r1, s1, d1 = cpu_oracle_rate(inp, k, n_single, 1)
+    rn, sn, dn = cpu_oracle_rate(inp, k, n_all, cores)
+    return {"value": r1, "unit": UNIT, "cores": 1, "threads": 1, "cpu": host_cpu(),
+            "kind": "oracle", "sample": d1, "seconds": s1,
+            "single_thread": {"value": r1, "threads": 1, "seconds": s1, "sample": d1},
+            "all_cores": {"value": rn, "threads": cores, "cores": cores, "seconds": sn,
+                          "sample": dn},
+            "how": ("oracle in a child process with OMP/OPENBLAS/MKL thread counts set to "
+                    "1 (single_thread) and to the host's cores (all_cores)")}
 
 
 def run_reference(args):
@@ -287,6 +347,7 @@ def run_reference(args):
         pairs += p
         secs += s
     value = pairs / secs
+    # one chunk at the measured rate (the oracle scores only a sample of it)
     ms_per_chunk = wl.visible_pairs / value * 1e3
     cores = os.cpu_count()
     line = {
@@ -294,8 +355,13 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_chunk,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded hot-key/topic generator)",
+        "ms_per_step_is_extrapolated": True,
+        "measured_ms_per_step": secs / args.steps * 1e3,
+        "extrapolation": (f"ms_per_step = one whole chunk ({wl.visible_pairs} visible pairs) at the "
+                          f"measured rate; each timed step scores {args.ref_queries} queries"),
         "config": {"workload": f"{args.workload} chunk, {args.dtype} inputs widened to fp64, k={wl.k}",
-                   "sample": f"{args.ref_queries} random queries of the chunk per step"},
+                   "sample": f"{args.ref_queries} random queries of the chunk per step",
+                   "threads": "numpy's default BLAS pool (all host cores)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cpu": host_cpu(), "kind": "oracle",
                          "sample": f"{args.ref_queries} queries per step x {args.steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -437,22 +503,18 @@ def run_retrieval(args):
 DECODE_METRIC = "decode: scored query-key pairs/s and ms per call, T new tokens at 1M ctx, k=2048 (1 GB300)"
 
 
-def run_decode(args):
-    """Decode / small-T: T queries (default 1) at the end of a 1M-token cache,
-    previous-step sample; the key range is split over the GPU."""
-    import numpy as np
+def decode_record(T: int, dtype: str, engine: str, steps: int, warmup: int, dev, rank: int = 0,
+                  world: int = 1) -> dict:
+    """Decode / small-T: T queries at the end of a 1M-token cache, previous-step
+    sample; the key range is split over the GPU.  Returns the JSON record."""
     import torch
     from indexer_topk_long_gb300 import IndexerTopK, datagen
-    rank, world, local = dist_env()
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    T = args.queries or 1
     S = 1 << 20
     keys = datagen.keys_fp32(S, 128, 20260715 + rank)
-    inp = datagen.make_indexer_inputs(T, S - T, S, dtype=args.dtype, seed=20260715 + rank, keys=keys)
+    inp = datagen.make_indexer_inputs(T, S - T, S, dtype=dtype, seed=20260715 + rank, keys=keys)
     d = to_dev(inp, torch, dev)
-    op = IndexerTopK(max_T=T, max_S=S, k=2048, dtype=args.dtype,
-                     engine={"auto": 0, "tensor": 1, "cuda": 2}[args.engine])
+    op = IndexerTopK(max_T=T, max_S=S, k=2048, dtype=dtype,
+                     engine={"auto": 0, "tensor": 1, "cuda": 2}[engine])
     out = (torch.empty((T, 2048), dtype=torch.int32, device=dev),
            torch.empty((T, 2048), dtype=torch.float32, device=dev))
     first = op(d["q"], d["w"], d["k_cache"], d["positions"], k=2048, q_scale=d["q_scale"], k_scale=d["k_scale"])
@@ -460,19 +522,19 @@ def run_decode(args):
     stream = torch.cuda.current_stream()
     step = lambda: op(d["q"], d["w"], d["k_cache"], d["positions"], k=2048, prev_topk=sample,
                       q_scale=d["q_scale"], k_scale=d["k_scale"], out=out)
-    for _ in range(max(args.warmup, 0)):
+    for _ in range(max(warmup, 0)):
         step()
     torch.cuda.synchronize()
     op.set_timing(True)
     launches0 = op.stats()["launches"]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
     st = op.stats()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     pairs = st["visible_pairs"]
     # the same call captured once in a CUDA graph and replayed (no launch gaps)
     op.set_timing(False)
@@ -485,23 +547,23 @@ def run_decode(args):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         step()
-    for _ in range(max(args.warmup, 1)):
+    for _ in range(max(warmup, 1)):
         graph.replay()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    graph_ms = e0.elapsed_time(e1) / args.steps
+    graph_ms = e0.elapsed_time(e1) / steps
     # a few queries against the whole cache: the key stream (S x d elements,
     # plus the fp8 scales) is the algorithmic traffic of the filter kernel
     peaks, kind = measured_peaks()
-    k_bytes = S * 128 * (1 if args.dtype == "fp8" else 2) + (S * 4 if args.dtype == "fp8" else 0)
+    k_bytes = S * 128 * (1 if dtype == "fp8" else 2) + (S * 4 if dtype == "fp8" else 0)
     flop = 16384.0 * pairs                         # H * d * 2 per visible pair (one call)
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     tflops = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    if args.dtype == "fp8":
+    if dtype == "fp8":
         tflops *= FP8_OVER_BF16
     # the bound is whichever floor is higher: streaming the cache or the MMAs
     t_hbm = k_bytes / (hbm * 1e9)
@@ -512,12 +574,12 @@ def run_decode(args):
     else:
         bound, achieved, peak, unit = "tensor", flop / sec / 1e12, tflops, "TFLOP/s"
     line = {"metric": DECODE_METRIC, "value": world * pairs / (ms * 1e-3), "unit": UNIT,
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+            "n_gpus": world, "steps": steps, "warmup": warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
             "data": "synthetic (seeded hot-key/topic generator)",
             "config": {"workload": f"decode: T={T} queries at positions {S - T}..{S - 1}, S={S}, H=64, "
                                    f"d=128, k=2048, previous-step sample; keys split over the GPU",
-                       "engine": args.engine},
+                       "engine": engine},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                          "frac": achieved / peak, "traffic": None,
                          "kernel": "filter stage (score_tc_kernel<filter>, keys split over the GPU)",
@@ -529,38 +591,62 @@ def run_decode(args):
             "graph": {"ms_per_step": graph_ms, "value": world * pairs / (graph_ms * 1e-3),
                       "how": "one call captured with torch.cuda.graph, replayed back to back"}}
     op.close()
+    del graph, d, out, first, sample
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_decode(args):
+    import torch
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    line = decode_record(args.queries or 1, args.dtype, args.engine, args.steps, args.warmup, dev,
+                         rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
 
 
-def main():
-    args = parse_args()
-    if args.impl == "reference":
-        return run_reference(args)
-    if args.workload == "retrieval":
-        return run_retrieval(args)
-    if args.workload == "decode":
-        return run_decode(args)
-    import numpy as np
+def clock_normalised(achieved: float, peak: float, clocks, peaks) -> float | None:
+    """achieved / (peak scaled to this run's SM clock): the measured tensor
+    peak was taken at its own median SM clock under load, this run at
+    another, and tensor throughput scales with the SM clock."""
+    try:
+        peak_mhz = float(peaks["clocks_under_load"]["sm_mhz_median"])
+        run_mhz = float(clocks["sm_mhz"])
+    except (KeyError, TypeError, ValueError):
+        return None
+    if peak_mhz <= 0 or run_mhz <= 0:
+        return None
+    return achieved / (peak * run_mhz / peak_mhz)
+
+
+def device_uuid(torch, dev):
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        return None
+
+
+def prefill_record(workload: str, dtype: str, steps: int, warmup: int, dev, *, rank: int = 0,
+                   world: int = 1, queries: int = 0, e2e: bool = True, decoupled: bool = True,
+                   dec_steps: int = 3, cpu: bool = False, cpu_queries: int = 64,
+                   cpu_single_queries: int = 16, litedsa: bool = True) -> dict:
+    """One prefill chunk (previous chunk first, its output is the sample): the
+    timed fused path, its roofline, and optionally the end-to-end host-buffer
+    call, the same-GPU decoupled baseline and the CPU oracle baseline."""
     import torch
     from indexer_topk_long_gb300 import IndexerTopK
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-
     seed = 20260715 + rank        # each rank runs its own, independent chunk
-    wl, inp, inp_prev = build_inputs(args.workload, args.dtype, seed, args.queries)
+    wl, inp, inp_prev = build_inputs(workload, dtype, seed, queries)
     d = to_dev(inp, torch, dev)
     dp = to_dev(inp_prev, torch, dev)
     k = wl.k
-    op = IndexerTopK(max_T=wl.T, max_S=wl.S, k=k, dtype=args.dtype,
-                     enable_decoupled=0, enable_host_io=0 if args.no_e2e else 1)
+    op = IndexerTopK(max_T=wl.T, max_S=wl.S, k=k, dtype=dtype,
+                     enable_decoupled=0, enable_host_io=1 if e2e else 0)
     stream = torch.cuda.current_stream()
 
     # previous chunk (its output provides the sample), outside the timed region
@@ -575,20 +661,14 @@ def main():
         op(d["q"], d["w"], d["k_cache"], d["positions"], k=k, prev_topk=sample,
            q_scale=d["q_scale"], k_scale=d["k_scale"], out=(out_idx, out_score))
 
-    for _ in range(max(args.warmup, 0)):
+    for _ in range(max(warmup, 0)):
         step()
     torch.cuda.synchronize()
     warm = op.stats()
     if warm["device_status"] != 0:
         raise RuntimeError(f"device status {warm['device_status']}")
 
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-    except Exception:
-        pass
-    clocks = ClockSampler(uuid)
+    clocks = ClockSampler(device_uuid(torch, dev))
     launches0 = op.stats()["launches"]
     op.set_timing(True)
     if world > 1:
@@ -598,7 +678,7 @@ def main():
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -612,31 +692,37 @@ def main():
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     pairs_step = st["visible_pairs"]
     assert pairs_step == wl.visible_pairs, (pairs_step, wl.visible_pairs)
-    ms_per_step = elapsed_ms / args.steps
-    value = whole_job_value(pairs_step, args.steps, world, elapsed_ms)
+    assert st["device_status"] == 0, st
+    ms_per_step = elapsed_ms / steps
+    value = whole_job_value(pairs_step, steps, world, elapsed_ms)
 
     peaks, peaks_kind = measured_peaks()
     bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    peak = bf16_peak * (FP8_OVER_BF16 if args.dtype == "fp8" else 1.0)
+    peak = bf16_peak * (FP8_OVER_BF16 if dtype == "fp8" else 1.0)
     achieved = FLOP_PER_PAIR * pairs_step / (st["ms_filter"] * 1e-3) / 1e12
-    traffic = recorded_traffic(f"score_filter_{args.workload}_{args.dtype}")
+    traffic = recorded_traffic(f"score_filter_{workload}_{dtype}")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
+                "frac": achieved / peak,
+                "frac_clock_normalised": clock_normalised(achieved, peak, clock_info, peaks),
+                "traffic": traffic,
                 "kernel": "score_tc_kernel<filter> (fused score + bin + gate + write-back)",
                 "peak_source": (f"{peaks_kind} bf16 sustained" +
-                                (" x 2 (nominal fp8/bf16 ratio)" if args.dtype == "fp8" else "")),
+                                (" x 2 (nominal fp8/bf16 ratio)" if dtype == "fp8" else "")),
+                "clock_normalisation": ("peak x (this run's median SM MHz / the median SM MHz "
+                                        "under load recorded with the measured peak)"),
                 "algorithmic_flop_per_launch": FLOP_PER_PAIR * pairs_step}
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded hot-key/topic generator; no dataset)",
         "config": {
-            "workload": (f"{args.workload} prefill chunk: T={wl.T} queries at positions "
+            "workload": (f"{workload} prefill chunk: T={wl.T} queries at positions "
                          f"{wl.first_pos}..{wl.first_pos + wl.T - 1}, S={wl.S}, H={wl.H}, "
-                         f"d={wl.d}, k={k}, {args.dtype} q/k, fp32 w, previous-chunk top-3k sample"),
-            "l2": "inputs larger than L2 (key cache 256 MiB bf16 > 129 MB L2)",
+                         f"d={wl.d}, k={k}, {dtype} q/k, fp32 w, previous-chunk top-3k sample"),
+            "l2": (f"inputs larger than L2 (key cache {wl.S * wl.d * (1 if dtype == 'fp8' else 2) / 2**20:.0f} MiB"
+                   f" + queries {wl.T * wl.H * wl.d * (1 if dtype == 'fp8' else 2) / 2**20:.0f} MiB > 129 MB L2)"),
             "parallelism": f"replicas: {world} independent chunks, one per GPU",
             "visible_pairs_per_chunk": pairs_step,
         },
@@ -654,20 +740,21 @@ def main():
     }
 
     # ---- LiteDSA packing of the chunk's output (groups of 8 neighbouring queries)
-    from indexer_topk_long_gb300 import litedsa_pack
-    litedsa_pack(out_idx, 8)
-    torch.cuda.synchronize()
-    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    l0.record(stream)
-    _, lens, _ = litedsa_pack(out_idx, 8)
-    l1.record(stream)
-    torch.cuda.synchronize()
-    line["litedsa"] = {"group": 8, "ms": l0.elapsed_time(l1),
-                       "kv_rows_packed": int(lens.sum().item()), "kv_rows_per_query_lists": wl.T * k,
-                       "kv_row_ratio": float(lens.sum().item()) / (wl.T * k)}
+    if litedsa:
+        from indexer_topk_long_gb300 import litedsa_pack
+        litedsa_pack(out_idx, 8)
+        torch.cuda.synchronize()
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        _, lens, _ = litedsa_pack(out_idx, 8)
+        l1.record(stream)
+        torch.cuda.synchronize()
+        line["litedsa"] = {"group": 8, "ms": l0.elapsed_time(l1),
+                           "kv_rows_packed": int(lens.sum().item()), "kv_rows_per_query_lists": wl.T * k,
+                           "kv_row_ratio": float(lens.sum().item()) / (wl.T * k)}
 
     # ---- end to end through the host-buffer C-ABI call
-    if not args.no_e2e:
+    if e2e:
         sample = op.make_sample(prev_idx, wl.S, 3 * k).cpu().pin_memory()
         host = {key: (v.cpu().pin_memory() if v is not None else None) for key, v in d.items()}
         hout = (torch.empty((wl.T, k), dtype=torch.int32, pin_memory=True),
@@ -682,7 +769,7 @@ def main():
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
@@ -690,17 +777,18 @@ def main():
         h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None) + \
             sample.numel() * 4
         d2h = sum(v.numel() * v.element_size() for v in hout)
-        line["e2e"] = {"value": whole_job_value(pairs_step, args.steps, world, e_ms), "unit": UNIT,
+        line["e2e"] = {"value": whole_job_value(pairs_step, steps, world, e_ms), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": e_ms / args.steps,
+                       "ms_per_step": e_ms / steps,
                        "call": "ltk_indexer_topk_host (pinned host buffers, copies inside)"}
         ok = torch.equal(hout[0], out_idx.cpu())
         line["e2e"]["matches_device_call"] = bool(ok)
         del host
 
     # ---- same-GPU decoupled baseline (materialise fp32 scores, then select)
-    if not args.no_decoupled and world == 1:
-        dec = IndexerTopK(max_T=wl.T, max_S=wl.S, k=k, dtype=args.dtype, enable_decoupled=1)
+    op.close()
+    if decoupled and world == 1:
+        dec = IndexerTopK(max_T=wl.T, max_S=wl.S, k=k, dtype=dtype, enable_decoupled=1)
         di = torch.empty_like(out_idx)
         ds = torch.empty_like(out_score)
         def dec_step():
@@ -709,7 +797,7 @@ def main():
         dec_step()
         torch.cuda.synchronize()
         dec.set_timing(True)
-        n_dec = max(1, min(args.steps, 3))
+        n_dec = max(1, min(steps, dec_steps))
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
@@ -725,16 +813,64 @@ def main():
                              "fused_speedup": dec_ms / ms_per_step,
                              "identical_output": bool(torch.equal(di, out_idx) and torch.equal(ds, out_score))}
         dec.close()
-        del dec
-        torch.cuda.empty_cache()
+        del dec, di, ds
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
-    if not args.no_cpu and world == 1 and rank == 0:
-        rate, secs, desc = cpu_oracle_rate(inp, k, args.cpu_queries)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(), "cpu": host_cpu(),
-                                "kind": "oracle", "sample": desc, "seconds": secs}
+    if cpu and world == 1 and rank == 0:
+        line["cpu_baseline"] = cpu_baseline_record(inp, k, cpu_single_queries, cpu_queries)
 
-    op.close()
+    del d, dp, out_idx, out_score, prev_idx
+    torch.cuda.empty_cache()
+    return line
+
+
+def sub_record(line: dict) -> dict:
+    """The keys of a sub-workload's record that the headline line nests."""
+    keep = ("ms_per_step", "value", "unit", "dtype", "steps", "warmup", "config", "roofline",
+            "stages_ms", "clocks", "candidates_per_query", "n_overflow", "decoupled", "graph",
+            "gpu_launches")
+    return {key: line[key] for key in keep if key in line}
+
+
+def main():
+    args = parse_args()
+    if args.oracle_child:
+        return oracle_child(args.oracle_child)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.workload == "retrieval":
+        return run_retrieval(args)
+    if args.workload == "decode":
+        return run_decode(args)
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    line = prefill_record(args.workload, args.dtype, args.steps, args.warmup, dev, rank=rank,
+                          world=world, queries=args.queries, e2e=not args.no_e2e,
+                          decoupled=not args.no_decoupled, cpu=not args.no_cpu,
+                          cpu_queries=args.cpu_queries, cpu_single_queries=args.cpu_single_queries)
+
+    # ---- the other configurations, measured in the same run (one GPU only):
+    # the 1M chunk in e4m3, the 256K chunk against its decoupled baseline
+    # (the pages compare the two at 256K and 1M), and decode at T = 1
+    headline = (args.workload == "1m" and args.dtype == "bf16" and not args.queries)
+    if headline and not args.no_extra and world == 1:
+        extra_steps, extra_warm = max(1, min(args.steps, 5)), max(2, min(args.warmup, 3))
+        line["fp8_1m"] = sub_record(prefill_record(
+            "1m", "fp8", extra_steps, extra_warm, dev, e2e=False, decoupled=not args.no_decoupled,
+            dec_steps=2, litedsa=False))
+        line["prefill_256k"] = sub_record(prefill_record(
+            "256k", "bf16", extra_steps, extra_warm, dev, e2e=False, decoupled=not args.no_decoupled,
+            dec_steps=3, litedsa=False))
+        line["decode_t1"] = sub_record(decode_record(1, "bf16", "auto", max(args.steps, 10),
+                                                     extra_warm, dev))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define LTK_ABI_VERSION 1
+#define LTK_ABI_VERSION 2
 
 typedef enum {
   LTK_OK = 0,
@@ -263,16 +263,25 @@ ltk_status ltk_decoupled_topk(ltk_handle* h, const void* q, const float* q_scale
  * mask.  Its scratch, the T x S fp32 score matrix, lives in a static device
  * array of 4,194,304 floats (16 MiB) that every GPU loading the library
  * holds until process exit; T * S above that returns LTK_ERR_ARG.  The
- * caller still owns all inputs and outputs.  The first call on each device
- * looks up that array's device address (with the device current), so make
- * the first call on a device before any stream capture.  All calls share the
- * array, so calls that overlap on the GPU race and corrupt each other's
- * results: serialise them (one stream, or synchronise between calls).
+ * caller still owns all inputs and outputs.
+ *   device_status  device int (4-byte aligned, caller-owned) or NULL.  The
+ *                  call zeroes it on the stream; a bounded wait in the scorer
+ *                  that expires (about 2 s) stores LTK_ERR_TIMEOUT there, and
+ *                  the outputs of that call are then undefined.  Read it after
+ *                  the stream has finished the call.  With NULL such an error
+ *                  is not reported anywhere.
+ * Each call looks up the array's device address with the caller's device
+ * current (no allocation); the first call on a device also loads the
+ * library's kernels there and sets their attributes, so make it before any
+ * stream capture.  All calls share the array, so calls that overlap on the
+ * GPU race and corrupt each other's results: serialise them (one stream, or
+ * synchronise between calls).
  */
 ltk_status ltk_decoupled_topk_noalloc(int dtype, int causal, const void* q, const float* q_scale,
                                       const float* w, const void* k_cache, const float* k_scale,
                                       const int* positions, int T, long long S, int k,
-                                      int* out_idx, float* out_score, void* stream);
+                                      int* out_idx, float* out_score, int* device_status,
+                                      void* stream);
 
 /*
  * LiteDSA candidate packing (LiteTopK arXiv abstract: LiteDSA packs the

@@ -387,6 +387,7 @@ __global__ void __launch_bounds__(THREADS) sample_stats_kernel(const SampleStats
       const float hi = __fadd_rn(mx, span);
       delta = __fdiv_rn(static_cast<float>(p.nb - 3), __fsub_rn(hi, sk));
       if (!(delta <= 1e30f)) delta = 1e30f;
+      if (p.pow2_delta) delta = pow2_floor(delta);   // wider bins: the span still fits
       smin = __fsub_rn(sk, __fdiv_rn(3.f, delta));
       theta = max(0, bin_of(sk, smin, delta, p.nb) - 1);
       ranged = true;
@@ -398,6 +399,7 @@ __global__ void __launch_bounds__(THREADS) sample_stats_kernel(const SampleStats
     if (mx > mn) {
       delta = __fdiv_rn(static_cast<float>(p.nb), __fmul_rn(2.f, __fsub_rn(mx, mn)));
       if (!(delta <= 1e30f)) delta = 1e30f;
+      if (p.pow2_delta) delta = pow2_floor(delta);
     }
   }
   if (threadIdx.x == 0) {

@@ -6,10 +6,16 @@
 // bin space through the inverse affine map).
 //
 // With w'[h] = w[h] * delta (and, for e4m3, times q_scale) the kernel forms
-//     B = sum_h w'[h] * f(q[h] . k) * k_scale - s_min * delta     (f = ReLU or id)
+//     V = sum_h w'[h] * f(q[h] . k) * k_scale   (f = ReLU or id),
+//     B = V - s_min * delta
 // directly; bin = clamp(floor(B), 0, nb - 1), the gate is bin >= theta, and a
-// kept candidate stores I = B / delta + s_min.  Dense mode (sample scoring,
-// decoupled baseline) forms I itself with the unscaled weights.
+// kept candidate stores I = V / delta.  The sample stage rounds delta down to
+// a power of two for this kernel, so w * delta, s_min * delta and V / delta
+// are exact: V is exactly delta times the score the same sum forms with the
+// unscaled weights, the inverse map returns that score bit for bit (integer
+// inputs: the exact score), and B is the same fp32 value as the shared bin
+// map's (I - s_min) * delta.  Dense mode (sample scoring, decoupled baseline)
+// forms I itself with the unscaled weights.
 //
 // It serves any head count H <= 128 and head dim d (multiple of 8, <= 4096):
 // shapes the tensor-core kernels do not cover, and small decode batches.
@@ -160,6 +166,7 @@ __global__ void __launch_bounds__(kCcThreads)
     if (!(delta > 0.f)) {   // no spread in the sample: any monotone map will do
       delta = 1.f;
     }
+    delta = pow2_floor(delta);   // already a power of two from the sample stage
   }
   for (int h = tid; h < p.H; h += kCcThreads) {
     float w = p.w[static_cast<size_t>(t) * p.H + h];
@@ -188,7 +195,7 @@ __global__ void __launch_bounds__(kCcThreads)
 
   if (warp < kCcComputeWarps) {
     const float c0 = ctrl.c0;
-    const float inv_delta = 1.f / delta;
+    const float inv_delta = __fdiv_rn(1.f, delta);
     for (int it = 0; it < n_steps; ++it) {
       const long long base = k_lo + it * keys_per_step + 2ll * tid;
       const bool ok0 = base < k_hi, ok1 = base + 1 < k_hi;
@@ -225,8 +232,8 @@ __global__ void __launch_bounds__(kCcThreads)
             slot0 = __shfl_sync(0xFFFFFFFFu, slot0, leader);
             if (pass) {
               const int slot = slot0 + __popc(m & ((1u << lane) - 1u));
-              // inverse affine map back to the score
-              const float I = __fmaf_rn(B, inv_delta, s_min);
+              // inverse affine map back to the score (exact: delta is a power of two)
+              const float I = __fmul_rn(v, inv_delta);
               if (slot < p.cap) p.cand[static_cast<size_t>(t) * p.cap + slot] = cand_pack(I, static_cast<int>(key));
               atomicAdd(&hist[b], 1);
             }

@@ -488,7 +488,8 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   sp.status = h->status;
   plan_work(h, a.T, n_pad, true, &sp.b_full, &sp.s_last, &qpu);
   LTK_CUDA(launch_scorer(h, kModeDense, q_map, ks_map, sp, st));
-  SampleStatsParams stp{h->samp_scores, n_pad, n_pad, a.T, a.k, c.n_bins, h->s_min, h->delta, h->theta0};
+  SampleStatsParams stp{h->samp_scores, n_pad, n_pad, a.T, a.k, c.n_bins, h->s_min, h->delta, h->theta0,
+                        use_cc(&c) ? 1 : 0};
   LTK_CUDA(launch_sample_stats(stp, h->num_sms, st));
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[1], st));
 
@@ -953,31 +954,18 @@ namespace {
 constexpr long long kNoAllocMaxScores = 4ll << 20;   // T * S <= 4,194,304 (16 MiB of fp32)
 static __device__ __align__(256) float g_noalloc_scores[kNoAllocMaxScores];
 
-constexpr int kNoAllocMaxDevices = 256;
-float* g_noalloc_ptr[kNoAllocMaxDevices] = {};      // device address of the array, per device
-
 // Host code must not use g_noalloc_scores directly: on the host it is only a
-// stand-in for the device symbol.  The device address is looked up once per
-// device, with that device current.
+// stand-in for the device symbol.  Its device address is looked up on every
+// call, with the caller's device current, so it stays right after a device
+// reset reloads the module.
 ltk_status noalloc_scores_for_current_device(float** out) {
-  static std::atomic<int> lock{0};
-  int dev = -1;
-  LTK_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return LTK_ERR_UNSUPPORTED;
-  while (lock.exchange(1, std::memory_order_acquire)) {
-  }
-  ltk_status st = LTK_OK;
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scores);
-    if (e == cudaSuccess && p != nullptr)
-      g_noalloc_ptr[dev] = static_cast<float*>(p);
-    else
-      st = cuda_fail(e == cudaSuccess ? cudaErrorInvalidSymbol : e, "cudaGetSymbolAddress");
-  }
-  *out = g_noalloc_ptr[dev];
-  lock.store(0, std::memory_order_release);
-  return st;
+  *out = nullptr;
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scores);
+  if (e != cudaSuccess || p == nullptr)
+    return cuda_fail(e == cudaSuccess ? cudaErrorInvalidSymbol : e, "cudaGetSymbolAddress");
+  *out = static_cast<float*>(p);
+  return LTK_OK;
 }
 
 }  // namespace
@@ -986,7 +974,8 @@ extern "C" ltk_status ltk_decoupled_topk_noalloc(int dtype, int causal, const vo
                                                  const float* q_scale, const float* w,
                                                  const void* k_cache, const float* k_scale,
                                                  const int* positions, int T, long long S, int k,
-                                                 int* out_idx, float* out_score, void* stream) {
+                                                 int* out_idx, float* out_score, int* device_status,
+                                                 void* stream) {
   if (dtype != LTK_BF16 && dtype != LTK_FP8_E4M3) return LTK_ERR_ARG;
   if (T < 0 || S < 1 || S > 0x7FFFFFFFll || k < 1 || k > kMaxK) return LTK_ERR_ARG;
   if (static_cast<long long>(T) * S > kNoAllocMaxScores) return LTK_ERR_ARG;
@@ -995,17 +984,25 @@ extern "C" ltk_status ltk_decoupled_topk_noalloc(int dtype, int causal, const vo
   if (!aligned16(q) || !aligned16(w) || !aligned16(k_cache) || !aligned16(out_idx) ||
       !aligned16(out_score))
     return LTK_ERR_ARG;
+  if (device_status != nullptr && (reinterpret_cast<uintptr_t>(device_status) & 3u) != 0)
+    return LTK_ERR_ARG;
   if (causal && (positions == nullptr || !aligned16(positions))) return LTK_ERR_ARG;
   const bool fp8 = dtype == LTK_FP8_E4M3;
   if (fp8 && (!q_scale || !k_scale || !aligned16(q_scale) || !aligned16(k_scale))) return LTK_ERR_ARG;
   float* scores = nullptr;
   const ltk_status st0 = noalloc_scores_for_current_device(&scores);
   if (st0 != LTK_OK) return st0;
+  int dev = 0, num_sms = 0;
+  LTK_CUDA(cudaGetDevice(&dev));
+  LTK_CUDA(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   CUtensorMap q_map, k_map;
   if (!make_tmap(&q_map, q, fp8, kTcDim, static_cast<unsigned long long>(T) * kTcHeads, 256) ||
       !make_tmap(&k_map, k_cache, fp8, kTcDim, static_cast<unsigned long long>(S), kTile))
     return LTK_ERR_CUDA;
+  // the caller's status word starts at zero; a bounded wait that expires in
+  // the scorer records LTK_ERR_TIMEOUT there
+  if (device_status != nullptr) LTK_CUDA(cudaMemsetAsync(device_status, 0, sizeof(int), st));
   ScoreParams sp{};
   sp.w = w;
   sp.q_scale = q_scale;
@@ -1017,9 +1014,9 @@ extern "C" ltk_status ltk_decoupled_topk_noalloc(int dtype, int causal, const vo
   sp.causal = causal ? 1 : 0;
   sp.dense = scores;
   sp.ld = S;
-  sp.status = nullptr;
-  sp.b_full = (T + kTcQPB - 1) / kTcQPB;
-  sp.s_last = 1;
+  sp.status = device_status;
+  // the same (query block, key range) work split as the handle's dense scorer
+  plan_split(T, S, num_sms, 2, &sp.b_full, &sp.s_last);
   LTK_CUDA(launch_score_tc(kModeDense, fp8, q_map, k_map, sp, st));
   RowTopkParams rp{scores, S, causal ? positions : nullptr, T, S, causal ? 1 : 0, k, out_idx,
                    out_score, nullptr};

@@ -418,7 +418,26 @@ struct SampleStatsParams {
   float* s_min;
   float* delta;
   int* theta0;
+  // 1: delta is rounded down to a power of two (the CUDA-core scorer scales
+  // its weights by delta, which is then exact, so its scores come back from
+  // bin space without rounding); 0: delta as computed.
+  int pow2_delta;
 };
+
+// Largest power of two <= x for a positive normal fp32 x (the exponent of x
+// with the mantissa cleared).
+__host__ __device__ __forceinline__ float pow2_floor(float x) {
+#ifdef __CUDA_ARCH__
+  return __uint_as_float(__float_as_uint(x) & 0xFF800000u);
+#else
+  uint32_t b;
+  __builtin_memcpy(&b, &x, 4);
+  b &= 0xFF800000u;
+  float r;
+  __builtin_memcpy(&r, &b, 4);
+  return r;
+#endif
+}
 
 // Sample stage (k_sample.cu).
 cudaError_t launch_random_sample(long long S, int n, unsigned long long seed, int* out,

@@ -104,33 +104,76 @@ def _e4m3_positive_table() -> np.ndarray:
 _E4M3_POS = _e4m3_positive_table()
 
 
+def _e4m3_codes_block(x: np.ndarray) -> np.ndarray:
+    """e4m3 codes of one block (float64 values, |x| <= 448 after saturation).
+
+    Normal range: the binary64 significand is rounded to 3 bits, ties to even
+    (adding 2^48 - 1 plus the kept LSB, then dropping 49 bits; a carry moves
+    into the exponent field), and the exponent is re-biased from 1023 to 7.
+    Below 2^-6 the e4m3 quantum is 2^-9, so the code is round-half-even of
+    |x| * 512.  Ties to the even value are ties to the even code."""
+    a = np.minimum(np.abs(x), 448.0)
+    b = a.view(np.uint64)
+    rb = (b + (np.uint64((1 << 48) - 1) + ((b >> np.uint64(49)) & np.uint64(1)))) >> np.uint64(49)
+    code = rb.astype(np.int64) - ((1023 - 7) << 3)
+    sub = a < 2.0 ** -6
+    code = np.where(sub, np.rint(a * 512.0).astype(np.int64), code).astype(np.uint8)
+    sign = (x < 0) & (code != 0)
+    return code | (sign.astype(np.uint8) << np.uint8(7))
+
+
+def _blocks(n: int, block: int):
+    return [(i, min(n, i + block)) for i in range(0, n, block)]
+
+
+def _threads() -> int:
+    import os
+    return max(1, min(16, os.cpu_count() or 1))
+
+
 def e4m3_codes(x: np.ndarray) -> np.ndarray:
     """float -> e4m3 codes (uint8), nearest value, ties to the even code.
 
     Magnitudes above 448 saturate to 448 (the generator never produces them,
-    since values are pre-divided by amax / 448).
-    """
-    x = np.asarray(x, dtype=np.float64)
-    a = np.minimum(np.abs(x), 448.0)
-    hi = np.searchsorted(_E4M3_POS, a, side="left")          # first value >= a
-    hi = np.minimum(hi, 0x7E)
-    lo = np.maximum(hi - 1, 0)
-    d_lo = a - _E4M3_POS[lo]
-    d_hi = _E4M3_POS[hi] - a
-    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0) & (hi != lo))
-    code = np.where(pick_hi, hi, lo).astype(np.uint8)
-    code = np.where(a == _E4M3_POS[hi], hi.astype(np.uint8), code)
-    sign = (x < 0) & (code != 0)
-    return (code | np.where(sign, 0x80, 0).astype(np.uint8)).astype(np.uint8)
+    since values are pre-divided by amax / 448).  Large arrays are encoded in
+    blocks on a thread pool (numpy releases the GIL)."""
+    flat = np.asarray(x, dtype=np.float64).reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    parts = _blocks(flat.size, 1 << 22)
+    if len(parts) <= 1:
+        out[:] = _e4m3_codes_block(flat)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+
+        def run(ab):
+            out[ab[0]:ab[1]] = _e4m3_codes_block(flat[ab[0]:ab[1]])
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(run, parts))
+    return out.reshape(np.shape(x))
 
 
 def fp8_quantize_rows(x: np.ndarray):
     """Per-row (per-token) e4m3 quantisation: returns (codes, scale fp32)."""
     x = np.asarray(x, dtype=np.float32)
     rows = x.reshape(x.shape[0], -1)
-    amax = np.abs(rows).max(axis=1).astype(np.float32)
-    scale = (np.maximum(amax, np.float32(1e-12)) / np.float32(448.0)).astype(np.float32)
-    codes = e4m3_codes(rows.astype(np.float64) / scale[:, None].astype(np.float64))
+    n, m = rows.shape
+    codes = np.empty((n, m), dtype=np.uint8)
+    scale = np.empty(n, dtype=np.float32)
+
+    def run(ab):
+        r = rows[ab[0]:ab[1]]
+        amax = np.abs(r).max(axis=1).astype(np.float32) if m else np.zeros(len(r), np.float32)
+        sc = (np.maximum(amax, np.float32(1e-12)) / np.float32(448.0)).astype(np.float32)
+        scale[ab[0]:ab[1]] = sc
+        codes[ab[0]:ab[1]] = _e4m3_codes_block(r.astype(np.float64) / sc[:, None].astype(np.float64))
+    parts = _blocks(n, max(1, (1 << 21) // max(m, 1)))
+    if len(parts) <= 1:
+        for ab in parts:
+            run(ab)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(run, parts))
     return codes.reshape(x.shape), scale
 
 

@@ -67,7 +67,7 @@ _SIGS = {
     "ltk_indexer_topk_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _LL, _P, _I, _I, _P, _P, _P]),
     "ltk_decoupled_topk": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _LL, _I, _P, _P, _P]),
     "ltk_get_stats": (_I, [_P, ctypes.POINTER(Stats)]),
-    "ltk_decoupled_topk_noalloc": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _I, _LL, _I, _P, _P, _P]),
+    "ltk_decoupled_topk_noalloc": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _I, _LL, _I, _P, _P, _P, _P]),
     "ltk_litedsa_pack": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
 }
 
@@ -216,6 +216,37 @@ def litedsa_pack(topk_idx, group: int, stream=None):
     _check(lib.ltk_litedsa_pack(_ptr(topk_idx), T, k, group, _ptr(union), _ptr(lens), _ptr(masks),
                                 _stream_handle(stream)), "ltk_litedsa_pack")
     return union, lens, masks
+
+
+def decoupled_noalloc(q, w, k_cache, positions=None, k: int = 2048, dtype: str = "bf16",
+                      causal: bool = True, q_scale=None, k_scale=None, out=None, status=None,
+                      stream=None):
+    """ltk_decoupled_topk_noalloc: the decoupled top-k (H = 64, d = 128) with its
+    score matrix in the library's static device array -- for callers that must
+    not allocate device memory (T * S <= 4,194,304).  Tensors are checked like
+    every other entry point's before the call.  Returns (idx int32 [T, k],
+    score fp32 [T, k], status int32 [1]); status holds LTK_ERR_TIMEOUT (5) once
+    the stream has run the call if a bounded device wait expired, else 0."""
+    import torch
+    lib = load_library()
+    k = int(k)
+    T, S = check_inputs(64, 128, dtype, causal, q, w, k_cache, positions, q_scale, k_scale,
+                        None, out, k, device_type="cuda", device_index=torch.cuda.current_device())
+    if out is None:
+        out = (torch.empty((T, k), dtype=torch.int32, device=q.device),
+               torch.empty((T, k), dtype=torch.float32, device=q.device))
+    if status is None:
+        status = torch.empty((1,), dtype=torch.int32, device=q.device)
+    _tensor_ok(status, "status", 1, 4, "cuda", dtype=torch.int32,
+               device_index=torch.cuda.current_device())
+    code = {"bf16": LTK_BF16, "fp8": LTK_FP8_E4M3}[dtype]
+    _check(lib.ltk_decoupled_topk_noalloc(code, 1 if causal else 0, _ptr(q), _ptr(q_scale), _ptr(w),
+                                          _ptr(k_cache), _ptr(k_scale),
+                                          _ptr(positions) if causal else None, T, S, k,
+                                          _ptr(out[0]), _ptr(out[1]), _ptr(status),
+                                          _stream_handle(stream)),
+           "ltk_decoupled_topk_noalloc")
+    return out[0], out[1], status
 
 
 class IndexerTopK:

@@ -46,9 +46,9 @@ int main(void) {
   ltk_stats st;
   expect(ltk_get_stats(NULL, &st) == LTK_ERR_ARG, "stats without a handle");
   expect(ltk_decoupled_topk_noalloc(7, 1, NULL, NULL, NULL, NULL, NULL, NULL, 1, 10, 1, NULL, NULL,
-                                    NULL) == LTK_ERR_ARG, "allocation-free call with a bad dtype");
+                                    NULL, NULL) == LTK_ERR_ARG, "allocation-free call with a bad dtype");
   expect(ltk_decoupled_topk_noalloc(LTK_BF16, 1, NULL, NULL, NULL, NULL, NULL, NULL, 4096, 4096, 1,
-                                    NULL, NULL, NULL) == LTK_ERR_ARG,
+                                    NULL, NULL, NULL, NULL) == LTK_ERR_ARG,
          "allocation-free call beyond its static array");
   expect(ltk_litedsa_pack(NULL, 4, 8, 0, NULL, NULL, NULL, NULL) == LTK_ERR_ARG, "LiteDSA group 0");
   expect(ltk_litedsa_pack(NULL, 4, 8192, 8, NULL, NULL, NULL, NULL) == LTK_ERR_UNSUPPORTED,

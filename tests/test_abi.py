@@ -16,7 +16,7 @@ def test_exports_every_declared_function(ltk_lib):
 
 
 def test_abi_version_and_status_strings(ltk_lib):
-    assert ltk_lib.ltk_abi_version() == 1
+    assert ltk_lib.ltk_abi_version() == 2
     assert ltk_lib.ltk_status_string(0) == b"ok"
     assert ltk_lib.ltk_status_string(5) == b"device wait timed out"
 

@@ -2,15 +2,16 @@
 inverse affine map) against the oracle, for the standard shape and for shapes
 the tensor-core kernels do not serve.
 
-Because w * delta is rounded before the head sum, this engine's scores differ
-from the plain formula by fp32 rounding even on integer inputs, so every case
-uses the floating-point tolerance rule.
+delta is a power of two on this engine, so w * delta and the inverse map are
+exact: on integer-valued inputs the results must match the oracle bit for bit,
+and the fused path must return exactly the decoupled (dense) path's scores.
+Floating-point inputs use the tolerance rule.
 """
 import numpy as np
 import pytest
 
 from indexer_topk_long_gb300 import IndexerTopK, datagen
-from parity import check_tolerant, to_device
+from parity import check_exact, check_tolerant, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -43,19 +44,36 @@ def test_standard_shape_on_cuda_cores():
 
 
 @pytest.mark.parametrize("H,d,dtype,integer", [(32, 64, "bf16", False), (16, 256, "fp8", False),
-                                               (8, 128, "bf16", True), (3, 40, "bf16", False)])
+                                               (8, 128, "bf16", True), (3, 40, "bf16", False),
+                                               (32, 64, "bf16", True), (64, 128, "bf16", True)])
 def test_other_shapes(H, d, dtype, integer):
     inp = datagen.make_indexer_inputs(T=13, first_pos=3000, S=3013, H=H, d=d, dtype=dtype,
                                       integer=integer, seed=H * d)
-    out = _run(inp, 512)
+    # (64, 128) is the tensor-core shape: force the CUDA-core engine there
+    out = _run(inp, 512, enable_decoupled=1, **({"engine": 2} if (H, d) == (64, 128) else {}))
     assert out["stats"]["n_overflow"] == 0
-    check_tolerant(inp, out["idx"], out["sc"], 512)
+    if integer:
+        check_exact(inp, out["idx"], out["sc"], 512)
+        check_exact(inp, out["dec_idx"], out["dec_sc"], 512)
+    else:
+        check_tolerant(inp, out["idx"], out["sc"], 512)
+    # the inverse map returns the dense path's own fp32 scores
+    np.testing.assert_array_equal(out["idx"], out["dec_idx"])
+    np.testing.assert_array_equal(out["sc"], out["dec_sc"])
 
 
 def test_decode_split_on_cuda_cores():
     inp = datagen.make_indexer_inputs(T=2, first_pos=199998, S=200000, H=32, d=64, seed=52)
     out = _run(inp, 2048)
     check_tolerant(inp, out["idx"], out["sc"], 2048)
+
+
+def test_decode_split_on_cuda_cores_integer():
+    """Key ranges split over many CTAs (global histogram), integer inputs: bit-exact."""
+    inp = datagen.make_indexer_inputs(T=3, first_pos=131069, S=131072, H=16, d=64, integer=True,
+                                      seed=54)
+    out = _run(inp, 2048)
+    check_exact(inp, out["idx"], out["sc"], 2048)
 
 
 def test_overflow_rescue_generic_shape():
