@@ -34,6 +34,15 @@ constexpr int kSelThreadsWide = 1024;   // few queries: one wide CTA each
 constexpr int kBndCap = 4096;        // boundary-bin entries held in shared memory
 constexpr int kRankSelect = 1024;    // boundary bins up to this size: select by rank counting
 
+// Bytes of the output-key buffer for k: the next power of two of k keys, at
+// least 1024 (the wide form's register sort holds 1024 keys at least).
+__host__ __device__ inline size_t outbuf_bytes(int k) {
+  int P = 1;
+  while (P < k) P <<= 1;
+  if (P < kSelThreadsWide) P = kSelThreadsWide;
+  return static_cast<size_t>(P) * sizeof(unsigned long long);
+}
+
 // ---------------------------------------------------------------------------
 // Block helpers
 // ---------------------------------------------------------------------------
@@ -572,11 +581,21 @@ __global__ void __launch_bounds__(THREADS) select_kernel(const SelectParams p) {
 // ---------------------------------------------------------------------------
 // Row top-k over a materialised score row (decoupled baseline and rescue)
 // ---------------------------------------------------------------------------
-// Radix select over the fp32 scores' order-preserving codes, 8 bits per pass,
-// reading the row from device memory once per pass; then one collection pass:
-// scores above the k-th go to the output, and among scores equal to the k-th
-// the lowest indices are kept (ordered scan).
-__device__ void row_topk_block(const float* row, int V, int kk, int k, int t, int* out_idx,
+// Bucket select over the value range, three reads of the row: (1) the row's
+// minimum and maximum; (2) a histogram of kRowBins equal-width bins over
+// [min, max] (the same monotone bin map as the Filter stage), which spreads
+// even concentrated scores over many bins, so plain shared-memory atomics
+// rarely collide; the bin holding the k-th score follows from a top-down scan;
+// (3) every score in a higher bin goes straight to the output, and the entries
+// of that bin are gathered, as (score, index) keys, into shared memory, where
+// the exact top of the bin is selected (ties to the lower index: the keys
+// order by score, then index).  A bin too crowded for shared memory (many
+// equal scores, or no spread) falls back to an 8-bit radix select over the
+// scores' order-preserving codes and an ordered collection of the ties.
+constexpr int kRowBins = 2048;
+constexpr int kRowCandCap = 4096;      // boundary-bin entries gathered in shared memory
+
+__device__ void row_topk_radix(const float* row, int V, int kk, int k, int t, int* out_idx,
                                float* out_score, unsigned long long* outbuf, unsigned* hist256,
                                long long* sh, int* sh_int) {
   if (kk <= 0) {
@@ -662,17 +681,209 @@ __device__ void row_topk_block(const float* row, int V, int kk, int k, int t, in
   write_sorted(outbuf, min(sh_int[0], kk), k, t, out_idx, out_score);
 }
 
-__global__ void __launch_bounds__(kSelThreads) row_topk_kernel(const RowTopkParams p) {
-  extern __shared__ unsigned long long rt_smem[];
+// Digit d of an nb-bin histogram (nb a multiple of the block size) with
+// count(bins > d) < remaining <= count(bins >= d): sh[0] = d,
+// sh[1] = count(bins > d).  Top-down block scan.
+__device__ void pick_digit_block(const unsigned* hist, int nb, long long remaining, long long* sh,
+                                 long long* warp_sums) {
+  const int per = nb / static_cast<int>(blockDim.x);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // thread i owns bins nb-1-(per*i) .. nb-per*(i+1), counted from the top
+  long long own = 0;
+  for (int r = 0; r < per; ++r) own += hist[nb - 1 - per * threadIdx.x - r];
+  long long cum = own;
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+    if (lane >= o) cum += n;
+  }
+  if (lane == 31) warp_sums[warp] = cum;
+  __syncthreads();
+  long long before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_sums[w];
+  cum += before;
+  const long long excl = cum - own;
+  if (excl < remaining && cum >= remaining) {
+    long long above = excl;
+    int digit = nb - per * (static_cast<int>(threadIdx.x) + 1);
+    for (int r = 0; r < per; ++r) {
+      const int d = nb - 1 - per * threadIdx.x - r;
+      const long long c = hist[d];
+      if (above + c >= remaining) {
+        digit = d;
+        break;
+      }
+      above += c;
+    }
+    sh[0] = digit;
+    sh[1] = above;
+  }
+  __syncthreads();
+}
+
+// Warp-aggregated slot reservation: every lane calls it; returns the slot of
+// a lane with take (-1 otherwise) from the shared counter ctr.
+__device__ __forceinline__ int reserve_slot(int* ctr, bool take) {
+  const unsigned m = __ballot_sync(0xFFFFFFFFu, take);
+  if (m == 0) return -1;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(ctr, __popc(m));
+  base = __shfl_sync(0xFFFFFFFFu, base, leader);
+  return take ? base + __popc(m & ((1u << lane) - 1u)) : -1;
+}
+
+__device__ void row_topk_block(const float* row, int V, int kk, int k, int t, int* out_idx,
+                               float* out_score, unsigned long long* outbuf,
+                               unsigned long long* cand, unsigned* hist, unsigned* hist256,
+                               long long* sh, long long* warp_sums, int* sh_int, float* red) {
+  if (kk <= 0) {
+    write_sorted(outbuf, 0, k, t, out_idx, out_score);
+    return;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  const int nv = vec ? (V >> 2) : 0;   // float4 part; the rest one by one
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  // (1) range of the row (four float4 loads in flight per thread)
+  float lo = INFINITY, hi = -INFINITY;
+  {
+    const int step = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + 3 * step < nv; i += 4 * step) {
+      const float4 x0 = __ldcs(r4 + i), x1 = __ldcs(r4 + i + step);
+      const float4 x2 = __ldcs(r4 + i + 2 * step), x3 = __ldcs(r4 + i + 3 * step);
+      lo = fminf(lo, fminf(fminf(fminf(x0.x, x0.y), fminf(x0.z, x0.w)), fminf(fminf(x1.x, x1.y), fminf(x1.z, x1.w))));
+      lo = fminf(lo, fminf(fminf(fminf(x2.x, x2.y), fminf(x2.z, x2.w)), fminf(fminf(x3.x, x3.y), fminf(x3.z, x3.w))));
+      hi = fmaxf(hi, fmaxf(fmaxf(fmaxf(x0.x, x0.y), fmaxf(x0.z, x0.w)), fmaxf(fmaxf(x1.x, x1.y), fmaxf(x1.z, x1.w))));
+      hi = fmaxf(hi, fmaxf(fmaxf(fmaxf(x2.x, x2.y), fmaxf(x2.z, x2.w)), fmaxf(fmaxf(x3.x, x3.y), fmaxf(x3.z, x3.w))));
+    }
+    for (; i < nv; i += step) {
+      const float4 x = __ldcs(r4 + i);
+      lo = fminf(fminf(lo, x.x), fminf(x.y, fminf(x.z, x.w)));
+      hi = fmaxf(fmaxf(hi, x.x), fmaxf(x.y, fmaxf(x.z, x.w)));
+    }
+  }
+  for (int i = (nv << 2) + threadIdx.x; i < V; i += blockDim.x) {
+    const float x = row[i];
+    lo = fminf(lo, x);
+    hi = fmaxf(hi, x);
+  }
+  lo = block_min(lo, red);
+  hi = block_max(hi, red);
+  const float span = __fsub_rn(hi, lo);
+  float scale = span > 0.f ? __fdiv_rn(static_cast<float>(kRowBins), span) : 0.f;
+  if (!(scale <= 1e30f)) scale = 1e30f;
+  // (2) histogram of the equal-width bins (two float4 loads in flight per thread)
+  for (int i = threadIdx.x; i < kRowBins; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  {
+    const int step = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + step < nv; i += 2 * step) {
+      const float4 x0 = __ldcs(r4 + i), x1 = __ldcs(r4 + i + step);
+      atomicAdd(&hist[bin_of(x0.x, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x0.y, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x0.z, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x0.w, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x1.x, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x1.y, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x1.z, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x1.w, lo, scale, kRowBins)], 1u);
+    }
+    for (; i < nv; i += step) {
+      const float4 x = __ldcs(r4 + i);
+      atomicAdd(&hist[bin_of(x.x, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x.y, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x.z, lo, scale, kRowBins)], 1u);
+      atomicAdd(&hist[bin_of(x.w, lo, scale, kRowBins)], 1u);
+    }
+  }
+  for (int i = (nv << 2) + threadIdx.x; i < V; i += blockDim.x)
+    atomicAdd(&hist[bin_of(row[i], lo, scale, kRowBins)], 1u);
+  __syncthreads();
+  pick_digit_block(hist, kRowBins, kk, sh, warp_sums);
+  const int bstar = static_cast<int>(sh[0]);
+  const int need = kk - static_cast<int>(sh[1]);   // entries taken from bin bstar (>= 1)
+  const unsigned in_bin = hist[bstar];
+  __syncthreads();
+  if (in_bin > static_cast<unsigned>(kRowCandCap)) {
+    row_topk_radix(row, V, kk, k, t, out_idx, out_score, outbuf, hist256, sh, sh_int);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    sh_int[0] = 0;   // output slots
+    sh_int[1] = 0;   // gathered bin entries
+  }
+  __syncthreads();
+  // (3) higher bins -> output; bin bstar -> shared memory.  A float4 whose
+  // largest score is below tau (the smallest score whose bin reaches bstar,
+  // found by bisection over the fp32 order: the same decision as the bin
+  // test) needs no further work, and a warp skips on one vote.
+  if (threadIdx.x == 0) {
+    // over the row's own range [lo, hi] (finite, and bin_of(hi) is the top bin)
+    uint32_t a = ord_f32(lo), b = ord_f32(hi);   // invariant: bin_of(unord(b)) >= bstar
+    while (a < b) {
+      const uint32_t mid = a + (b - a) / 2;
+      if (bin_of(unord_f32(mid), lo, scale, kRowBins) >= bstar) b = mid; else a = mid + 1;
+    }
+    sh_int[2] = static_cast<int>(a);
+  }
+  __syncthreads();
+  const uint32_t tau_ord = static_cast<uint32_t>(sh_int[2]);
+  auto take_one = [&](float sv, int i, bool ok) {
+    const int b = bin_of(sv, lo, scale, kRowBins);
+    const int so = reserve_slot(&sh_int[0], ok && b > bstar);
+    if (so >= 0 && so < kk) outbuf[so] = ckey(sv, i);
+    const int sc = reserve_slot(&sh_int[1], ok && b == bstar);
+    if (sc >= 0 && sc < kRowCandCap) cand[sc] = ckey(sv, i);
+  };
+  for (int base = warp * 32; base < nv; base += nw * 32) {
+    const int i4 = base + lane;
+    const bool ok = i4 < nv;
+    const float4 x = ok ? __ldcs(r4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const float mx = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+    if (!__any_sync(0xFFFFFFFFu, ok && ord_f32(mx) >= tau_ord)) continue;
+    take_one(x.x, 4 * i4 + 0, ok);
+    take_one(x.y, 4 * i4 + 1, ok);
+    take_one(x.z, 4 * i4 + 2, ok);
+    take_one(x.w, 4 * i4 + 3, ok);
+  }
+  for (int base = (nv << 2) + warp * 32; base < V; base += nw * 32) {   // the rest, one by one
+    const int i = base + lane;
+    const bool ok = i < V;
+    take_one(ok ? row[i] : 0.f, i, ok);
+  }
+  __syncthreads();
+  const int m = min(sh_int[1], kRowCandCap);
+  unsigned long long kth_key = 0ull;
+  if (need < m) kth_key = select_u64_smem(cand, m, need, hist256, sh);
+  __syncthreads();
+  for (int base = 0; base < m; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    const bool take = j < m && (need >= m || cand[j] >= kth_key);
+    const int so = reserve_slot(&sh_int[0], take);
+    if (so >= 0 && so < kk) outbuf[so] = cand[j];
+  }
+  __syncthreads();
+  write_sorted(outbuf, min(sh_int[0], kk), k, t, out_idx, out_score);
+}
+
+__global__ void __launch_bounds__(kSelThreads, 2) row_topk_kernel(const RowTopkParams p) {
+  extern __shared__ unsigned long long rt_smem[];   // [outbuf keys][kRowCandCap bin entries]
+  __shared__ unsigned hist[kRowBins];
   __shared__ unsigned hist256[256];
   __shared__ long long sh[2];
-  __shared__ int sh_int[2];
+  __shared__ long long warp_sums[kSelThreads / 32];
+  __shared__ int sh_int[3];
+  __shared__ float red[kSelThreads / 32];
   const int t = blockIdx.x;
   const int V = visible_of(p.positions, t, p.S, p.causal);
   const int kk = min(p.k, V);
   if (threadIdx.x == 0 && p.pairs != nullptr) atomicAdd(p.pairs, static_cast<unsigned long long>(V));
+  unsigned long long* cand = rt_smem + outbuf_bytes(p.k) / sizeof(unsigned long long);
   row_topk_block(p.rows + static_cast<size_t>(t) * p.ld, V, kk, p.k, t, p.out_idx, p.out_score,
-                 rt_smem, hist256, sh, sh_int);
+                 rt_smem, cand, hist, hist256, sh, warp_sums, sh_int, red);
 }
 
 // ---------------------------------------------------------------------------
@@ -827,9 +1038,12 @@ __device__ void rescue_row_scores(const RescueParams& p, int t, int V, float* ro
 
 __global__ void __launch_bounds__(kRescueThreads) rescue_kernel(const RescueParams p) {
   extern __shared__ unsigned long long rs_smem[];
+  __shared__ unsigned hist[kRowBins];
   __shared__ unsigned hist256[256];
   __shared__ long long sh[2];
-  __shared__ int sh_int[2];
+  __shared__ long long warp_sums[kRescueThreads / 32];
+  __shared__ int sh_int[3];
+  __shared__ float red[kRescueThreads / 32];
   __shared__ int s_slot;
   __shared__ float wf[128];
   float* qf = reinterpret_cast<float*>(rs_smem);   // [H*d] fp32, reused as output buffer later
@@ -844,17 +1058,13 @@ __global__ void __launch_bounds__(kRescueThreads) rescue_kernel(const RescuePara
     const int V = visible_of(p.positions, t, p.S, p.causal);
     const int kk = min(p.k, V);
     rescue_row_scores(p, t, V, row, qf, wf);
-    row_topk_block(row, V, kk, p.k, t, p.out_idx, p.out_score, rs_smem, hist256, sh, sh_int);
+    row_topk_block(row, V, kk, p.k, t, p.out_idx, p.out_score, rs_smem,
+                   rs_smem + outbuf_bytes(p.k) / sizeof(unsigned long long), hist, hist256, sh,
+                   warp_sums, sh_int, red);
     __syncthreads();
   }
 }
 
-size_t outbuf_bytes(int k) {
-  int P = 1;
-  while (P < k) P <<= 1;
-  if (P < kSelThreadsWide) P = kSelThreadsWide;   // the wide form's sort holds 1024 keys at least
-  return static_cast<size_t>(P) * sizeof(unsigned long long);
-}
 
 }  // namespace
 
@@ -885,9 +1095,10 @@ cudaError_t launch_select(const SelectParams& p, int num_sms, cudaStream_t strea
 
 cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream) {
   if (p.T <= 0) return cudaSuccess;
-  const size_t smem = outbuf_bytes(p.k);
+  const size_t cand_bytes = kRowCandCap * sizeof(unsigned long long);
+  const size_t smem = outbuf_bytes(p.k) + cand_bytes;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(row_topk_kernel), kSlotRowTopk,
-                                    outbuf_bytes(kMaxK));
+                                    outbuf_bytes(kMaxK) + cand_bytes);
   if (e != cudaSuccess) return e;
   row_topk_kernel<<<p.T, kSelThreads, smem, stream>>>(p);
   count_launches(1);
@@ -897,8 +1108,11 @@ cudaError_t launch_row_topk(const RowTopkParams& p, cudaStream_t stream) {
 cudaError_t launch_rescue(const RescueParams& p, int rescue_rows, cudaStream_t stream) {
   if (p.T <= 0 || rescue_rows <= 0) return cudaSuccess;
   const size_t qbytes = static_cast<size_t>(p.heads) * p.dim * sizeof(float);
-  const size_t smem = qbytes > outbuf_bytes(p.k) ? qbytes : outbuf_bytes(p.k);
-  const size_t mx = kCcMaxSmem > outbuf_bytes(kMaxK) ? kCcMaxSmem : outbuf_bytes(kMaxK);
+  const size_t cand_bytes = kRowCandCap * sizeof(unsigned long long);
+  const size_t sel = outbuf_bytes(p.k) + cand_bytes;
+  const size_t smem = qbytes > sel ? qbytes : sel;
+  const size_t sel_max = outbuf_bytes(kMaxK) + cand_bytes;
+  const size_t mx = kCcMaxSmem > sel_max ? kCcMaxSmem : sel_max;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(rescue_kernel), kSlotRescue, mx);
   if (e != cudaSuccess) return e;
   rescue_kernel<<<rescue_rows, kRescueThreads, smem, stream>>>(p);
