@@ -374,35 +374,30 @@ RETRIEVAL = dict(T=1024, N=8388608, d=768, k=1000, sample=3000)
 RETRIEVAL_METRIC = "scored query-vector pairs/s, vector retrieval 1024 x 8.4M, d=768 (1 GB300)"
 
 
-def run_retrieval(args):
+def retrieval_record(dev, steps: int, warmup: int, k: int = 0, corpus: int = 0, queries: int = 0,
+                     rank: int = 0, world: int = 1, e2e: bool = True, decoupled: bool = True,
+                     cpu: bool = True) -> dict:
     """Vector-retrieval workload: one head, plain inner product, no mask."""
     import numpy as np
     import torch
     from indexer_topk_long_gb300 import IndexerTopK, datagen
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
     R = dict(RETRIEVAL)
-    if args.k:
-        R["k"] = args.k
-        R["sample"] = min(3 * args.k, 16384)
-    if args.corpus:
-        R["N"] = args.corpus
-    T = args.queries or R["T"]
+    if k:
+        R["k"] = k
+        R["sample"] = min(3 * k, 16384)
+    if corpus:
+        R["N"] = corpus
+    T = queries or R["T"]
     q, c = datagen.retrieval_inputs_torch(R["N"], T, R["d"], seed=20260715 + rank, device=dev)
     w = torch.ones((T, 1), dtype=torch.float32, device=dev)
     qi, ci = q.view(torch.int16), c.view(torch.int16)
     op = IndexerTopK(max_T=T, max_S=R["N"], k=R["k"], heads=1, dim=R["d"], sample_size=R["sample"],
-                     enable_host_io=0 if args.no_e2e else 1)
+                     enable_host_io=1 if e2e else 0)
     stream = torch.cuda.current_stream()
     out = (torch.empty((T, R["k"]), dtype=torch.int32, device=dev),
            torch.empty((T, R["k"]), dtype=torch.float32, device=dev))
     step = lambda: op(qi, w, ci, None, k=R["k"], out=out)
-    for _ in range(max(args.warmup, 0)):
+    for _ in range(max(warmup, 0)):
         step()
     torch.cuda.synchronize()
     launches0 = op.stats()["launches"]
@@ -410,11 +405,11 @@ def run_retrieval(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(None)
+    clocks = ClockSampler(device_uuid(torch, dev))
     clocks.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
@@ -431,15 +426,16 @@ def run_retrieval(args):
     line = {
         "metric": (RETRIEVAL_METRIC if R["N"] == RETRIEVAL["N"]
                    else RETRIEVAL_METRIC.replace("8.4M", str(R["N"]))),
-        "value": whole_job_value(pairs, args.steps, world, elapsed),
-        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": elapsed / args.steps, "higher_is_better": True, "scaling": "weak",
+        "value": whole_job_value(pairs, steps, world, elapsed),
+        "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warmup,
+        "ms_per_step": elapsed / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (clustered Gaussian corpus; MSMARCO unavailable)",
         "config": {"workload": f"vector retrieval: {T} queries x {R['N']} corpus rows, d={R['d']}, "
                                f"k={R['k']}, H=1, no ReLU, no mask, {R['sample']} random sample rows",
                    "l2": f"inputs larger than L2 (corpus {R['N'] * R['d'] * 2 / 1e9:.1f} GB)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
+                     "frac_clock_normalised": clock_normalised(achieved, peak, clock_info, peaks),
                      "traffic": (recorded_traffic(f"retrieval_filter_8m_k{R['k']}", RETRIEVAL_SOURCES)
                                  if R["N"] == RETRIEVAL["N"] and T == RETRIEVAL["T"] else None),
                      "kernel": "retrieval_tc_kernel<filter>",
@@ -449,21 +445,28 @@ def run_retrieval(args):
                       "rescue": st["ms_rescue"]},
         "candidates_per_query": st["cand_written"] / T, "n_overflow": st["n_overflow"],
     }
-    if not args.no_decoupled and world == 1:
+    if decoupled and world == 1:
+        op.close()
         dec = IndexerTopK(max_T=T, max_S=R["N"], k=R["k"], heads=1, dim=R["d"], enable_decoupled=1)
         di, ds = dec.decoupled(qi, w, ci, None, k=R["k"])
         torch.cuda.synchronize()
+        dec.set_timing(True)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
         dec.decoupled(qi, w, ci, None, k=R["k"], out=(di, ds))
         a1.record(stream)
         torch.cuda.synchronize()
-        line["decoupled"] = {"ms_per_step": a0.elapsed_time(a1),
+        dst = dec.stats()
+        dec_ms = a0.elapsed_time(a1)
+        line["decoupled"] = {"ms_per_step": dec_ms, "score_kernel_ms": dst["ms_filter"],
+                             "select_ms": dst["ms_select"], "fused_speedup": dec_ms / line["ms_per_step"],
                              "identical_output": bool(torch.equal(di, out[0]) and torch.equal(ds, out[1]))}
         dec.close()
         del dec, di, ds
         torch.cuda.empty_cache()
-    if not args.no_e2e:
+        op = IndexerTopK(max_T=T, max_S=R["N"], k=R["k"], heads=1, dim=R["d"], sample_size=R["sample"],
+                         enable_host_io=1 if e2e else 0)
+    if e2e:
         hq, hw, hc = qi.cpu().pin_memory(), w.cpu().pin_memory(), ci.cpu().pin_memory()
         hout = (torch.empty((T, R["k"]), dtype=torch.int32, pin_memory=True),
                 torch.empty((T, R["k"]), dtype=torch.float32, pin_memory=True))
@@ -471,15 +474,15 @@ def run_retrieval(args):
         torch.cuda.synchronize()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             op.topk_host(hq, hw, hc, None, k=R["k"], out=hout)
         a1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(a0.elapsed_time(a1), dev)
-        line["e2e"] = {"value": whole_job_value(pairs, args.steps, world, e_ms), "unit": UNIT,
+        line["e2e"] = {"value": whole_job_value(pairs, steps, world, e_ms), "unit": UNIT,
                        "h2d_bytes_per_step": hq.numel() * 2 + hw.numel() * 4 + hc.numel() * 2,
-                       "d2h_bytes_per_step": T * R["k"] * 8, "ms_per_step": e_ms / args.steps}
-    if not args.no_cpu and world == 1 and rank == 0:
+                       "d2h_bytes_per_step": T * R["k"] * 8, "ms_per_step": e_ms / steps}
+    if cpu and world == 1 and rank == 0:
         import oracle.indexer_topk as orc
         n_rows = R["N"]   # the whole corpus (~10 s of widening and products on the host)
         sel = sorted({0, T // 3, (2 * T) // 3, T - 1})
@@ -489,10 +492,27 @@ def run_retrieval(args):
         orc.retrieval_topk(qh, ch, R["k"])
         secs = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": len(sel) * n_rows / secs, "unit": UNIT, "cores": os.cpu_count(),
-                                "cpu": host_cpu(),
+                                "threads": os.cpu_count(), "cpu": host_cpu(),
                                 "kind": "oracle", "seconds": secs,
                                 "sample": f"{len(sel)} queries against the whole corpus ({n_rows} rows)"}
     op.close()
+    del q, c, qi, ci, out
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_retrieval(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    line = retrieval_record(dev, args.steps, args.warmup, k=args.k, corpus=args.corpus,
+                            queries=args.queries, rank=rank, world=world, e2e=not args.no_e2e,
+                            decoupled=not args.no_decoupled, cpu=not args.no_cpu)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -859,7 +879,8 @@ def main():
 
     # ---- the other configurations, measured in the same run (one GPU only):
     # the 1M chunk in e4m3, the 256K chunk against its decoupled baseline
-    # (the pages compare the two at 256K and 1M), and decode at T = 1
+    # (the pages compare the two at 256K and 1M), decode at T = 1, and the
+    # vector-retrieval workload (1024 queries x 8.4M rows, k = 1000)
     headline = (args.workload == "1m" and args.dtype == "bf16" and not args.queries)
     if headline and not args.no_extra and world == 1:
         extra_steps, extra_warm = max(1, min(args.steps, 5)), max(2, min(args.warmup, 3))
@@ -871,6 +892,8 @@ def main():
             dec_steps=3, litedsa=False))
         line["decode_t1"] = sub_record(decode_record(1, "bf16", "auto", max(args.steps, 10),
                                                      extra_warm, dev))
+        line["retrieval"] = sub_record(retrieval_record(dev, extra_steps, extra_warm, e2e=False,
+                                                        decoupled=not args.no_decoupled, cpu=False))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
