@@ -20,8 +20,9 @@
 //   * Epilogue (16 warps, one per TMEM lane quarter and query of a group): the
 //     query's 64 columns come in four tcgen05.ld 16x256b.x4 pieces, each in
 //     flight while the previous one is summed, and the accumulator goes back
-//     once the last piece has landed; ReLU and the w-weighted head sum run as
-//     packed fp32x2 FMAs with the weights in registers, a quad reduce-scatter
+//     once the last piece has landed; ReLU (x + |x| as a packed fp32x2 add)
+//     and the w-weighted head sum (packed fp32x2 FMAs, weights in registers)
+//     run two heads per instruction, a quad reduce-scatter
 //     leaves each thread one key -> mask -> [dense: store I] or [filter: bin,
 //     gate, warp ballot append, shared-memory histogram].
 //   * Warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warp 2 =
@@ -98,17 +99,23 @@ constexpr size_t smem_bytes(int nb) {
 // Partial weighted head sums of one query for 2 keys over 16 heads: v holds a
 // 16x256b x4 load (32 columns of 16 lanes), so thread t (c = t % 4) has heads
 // h = 8(roff + r) + 2c + {0, 1} of keys t/4 and t/4 + 8 for r = 0..3; w2 packs
-// the weights of each head pair.  Each packed FMA covers one head pair of one
-// key.  The even head's ReLU is max(x, 0) (ALU pipe); the odd head uses
-// x + |x| = 2 max(x, 0) (FMA pipe) and its accumulator half is halved at the
-// end (fold_pair), which is exact, so the sums equal sum_h w[h] * max(0, x[h])
-// accumulated in head order.
-__device__ __forceinline__ float relu_twice(float x) { return __fadd_rn(x, fabsf(x)); }
+// the weights of each head pair.  Per head pair and key, one packed add forms
+// (x0 + |x0|, x1 + |x1|) = 2 (max(0, x0), max(0, x1)) exactly (|x| is an
+// operand of the add) and one packed FMA accumulates it with the weights; the
+// two halves of the accumulator are added and halved at the end (fold_pair,
+// exact), so the sums equal sum_h w[h] * max(0, x[h]) up to fp32 rounding.
+__device__ __forceinline__ unsigned long long relu2_pair(float x0, float x1) {
+  unsigned long long x, ax, s;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ax) : "f"(fabsf(x0)), "f"(fabsf(x1)));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(x), "l"(ax));
+  return s;
+}
 
 __device__ __forceinline__ float fold_pair(unsigned long long acc) {
   const float lo = __uint_as_float(static_cast<uint32_t>(acc));
   const float hi = __uint_as_float(static_cast<uint32_t>(acc >> 32));
-  return __fmaf_rn(hi, 0.5f, lo);
+  return __fmul_rn(__fadd_rn(lo, hi), 0.5f);
 }
 
 __device__ __forceinline__ void head_partials(unsigned long long& a0, unsigned long long& a1,
@@ -116,8 +123,8 @@ __device__ __forceinline__ void head_partials(unsigned long long& a0, unsigned l
                                               const unsigned long long (&w2)[8], int roff) {
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    ffma2_acc(a0, fmaxf(v[4 * r + 0], 0.f), relu_twice(v[4 * r + 1]), w2[roff + r]);
-    ffma2_acc(a1, fmaxf(v[4 * r + 2], 0.f), relu_twice(v[4 * r + 3]), w2[roff + r]);
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a0) : "l"(relu2_pair(v[4 * r + 0], v[4 * r + 1])), "l"(w2[roff + r]));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a1) : "l"(relu2_pair(v[4 * r + 2], v[4 * r + 3])), "l"(w2[roff + r]));
   }
 }
 
