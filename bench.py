@@ -362,7 +362,8 @@ def run_reference(args):
         "config": {"workload": f"{args.workload} chunk, {args.dtype} inputs widened to fp64, k={wl.k}",
                    "sample": f"{args.ref_queries} random queries of the chunk per step",
                    "threads": "numpy's default BLAS pool (all host cores)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cpu": host_cpu(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "threads": cores, "cpu": host_cpu(),
+                         "kind": "oracle",
                          "sample": f"{args.ref_queries} queries per step x {args.steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
