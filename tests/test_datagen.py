@@ -59,3 +59,25 @@ def test_integer_mode_values():
     assert np.all(q == np.round(q)) and np.abs(q).max() <= 3
     assert np.all(k == np.round(k)) and np.abs(k).max() <= 3
     assert set(np.unique(inp.w).tolist()) <= {0.5, 0.25, 0.125, 0.0625}
+
+
+def test_e4m3_encoder_matches_torch_at_midpoints_and_in_blocks():
+    """The block encoder against torch's float8_e4m3fn conversion (round to
+    nearest, ties to even): every code's value, every midpoint between
+    neighbours (the ties), one float32 ulp either side of them, subnormals,
+    and an array large enough to go through the threaded block path.  The
+    points are float32 values (torch converts wider inputs through float32,
+    rounding twice), widened exactly for the encoder."""
+    torch = pytest.importorskip("torch")
+    pos = orc.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8)).astype(np.float32)   # 0 .. 448
+    mids = ((pos[:-1].astype(np.float64) + pos[1:]) / 2).astype(np.float32)      # exact in fp32
+    pts = np.concatenate([pos, mids, np.nextafter(mids, np.float32(0)),
+                          np.nextafter(mids, np.float32(1e9))])
+    pts = np.concatenate([pts, -pts, np.linspace(-2 ** -6, 2 ** -6, 1001, dtype=np.float32)])
+    big = np.clip(np.random.default_rng(2).standard_normal(5_000_000) * 60, -448, 448).astype(np.float32)
+    for x in (pts, big):
+        ours = datagen.e4m3_codes(x.astype(np.float64))
+        ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        # -0 and +0 are the same value; the generator writes +0
+        same = (ours == ref) | (((ours & 0x7F) == 0) & ((ref & 0x7F) == 0))
+        assert same.all(), x[~same][:8]
