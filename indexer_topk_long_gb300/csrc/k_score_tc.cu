@@ -17,14 +17,16 @@
 //     (one query group, half of the block): keys sit on TMEM lanes.  TMEM (512
 //     columns) holds two accumulators, one per group; the epilogue drains one
 //     while the tensor core fills the other.
-//   * Epilogue (16 warps, one per TMEM lane quarter and query of a group): the
-//     query's 64 columns come in four tcgen05.ld 16x256b.x4 pieces, each in
-//     flight while the previous one is summed, and the accumulator goes back
-//     once the last piece has landed; ReLU (x + |x| as a packed fp32x2 add)
-//     and the w-weighted head sum (packed fp32x2 FMAs, weights in registers)
-//     run two heads per instruction, a quad reduce-scatter
-//     leaves each thread one key -> mask -> [dense: store I] or [filter: bin,
-//     gate, warp ballot append, shared-memory histogram].
+//   * Epilogue (16 warps, one per TMEM lane quarter and query of a group):
+//     one thread per key row.  The query's 64 head columns of the thread's
+//     row come in four tcgen05.ld 32x32b.x16 pieces (the TMEM read shape with
+//     the highest bandwidth), each in flight while the previous one is summed,
+//     and the accumulator goes back once the last piece has landed; ReLU
+//     (x + |x| as a packed fp32x2 add) and the w-weighted head sum (packed
+//     fp32x2 FMAs, weights as shared-memory broadcasts) run two heads per
+//     instruction, and each thread ends with its key's whole score -> mask ->
+//     [dense: store I] or [filter: bin, gate, warp ballot append,
+//     shared-memory histogram].
 //   * Warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warp 2 =
 //     threshold refresh.
 //   * Work units: whole query blocks, or key ranges of a query block split
@@ -91,19 +93,11 @@ constexpr size_t smem_bytes(int nb) {
          static_cast<size_t>(kTcQPB) * nb * sizeof(int);
 }
 
-// One query's weighted head sum for the 32 keys of a warp's TMEM lane quarter:
-// the warp reads the query's 64 accumulator columns with two 16x256b loads
-// (lanes 0-15 and 16-31 of the quarter), so thread t (c = t % 4) holds 16
-// heads {8r + 2c + i} of the 4 keys t/4 + {0, 8, 16, 24}.
-//
-// Partial weighted head sums of one query for 2 keys over 16 heads: v holds a
-// 16x256b x4 load (32 columns of 16 lanes), so thread t (c = t % 4) has heads
-// h = 8(roff + r) + 2c + {0, 1} of keys t/4 and t/4 + 8 for r = 0..3; w2 packs
-// the weights of each head pair.  Per head pair and key, one packed add forms
-// (x0 + |x0|, x1 + |x1|) = 2 (max(0, x0), max(0, x1)) exactly (|x| is an
-// operand of the add) and one packed FMA accumulates it with the weights; the
-// two halves of the accumulator are added and halved at the end (fold_pair,
-// exact), so the sums equal sum_h w[h] * max(0, x[h]) up to fp32 rounding.
+// ReLU of a head pair, doubled: one packed add forms (x0 + |x0|, x1 + |x1|) =
+// 2 (max(0, x0), max(0, x1)) exactly (|x| is an operand of the add); a packed
+// FMA then accumulates it with the pair's weights, and the two halves of the
+// accumulator are added and halved at the end (fold_pair, exact), so the sums
+// equal sum_h w[h] * max(0, x[h]) up to fp32 rounding.
 __device__ __forceinline__ unsigned long long relu2_pair(float x0, float x1) {
   unsigned long long x, ax, s;
   asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
@@ -118,29 +112,20 @@ __device__ __forceinline__ float fold_pair(unsigned long long acc) {
   return __fmul_rn(__fadd_rn(lo, hi), 0.5f);
 }
 
-__device__ __forceinline__ void head_partials(unsigned long long& a0, unsigned long long& a1,
-                                              const float (&v)[16],
-                                              const unsigned long long (&w2)[8], int roff) {
+// Weighted ReLU sum over 16 consecutive heads of this thread's key (one
+// 32x32b x16 load): head pairs (4r, 4r+1) into a0 and (4r+2, 4r+3) into a1,
+// two heads per packed add and packed FMA; w points at the 16 weights.
+__device__ __forceinline__ void head_sum16(unsigned long long& a0, unsigned long long& a1,
+                                           const float (&x)[16], const float4* w) {
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a0) : "l"(relu2_pair(v[4 * r + 0], v[4 * r + 1])), "l"(w2[roff + r]));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a1) : "l"(relu2_pair(v[4 * r + 2], v[4 * r + 3])), "l"(w2[roff + r]));
+    const float4 wv = w[r];
+    unsigned long long w01, w23;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w01) : "f"(wv.x), "f"(wv.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w23) : "f"(wv.z), "f"(wv.w));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a0) : "l"(relu2_pair(x[4 * r + 0], x[4 * r + 1])), "l"(w01));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a1) : "l"(relu2_pair(x[4 * r + 2], x[4 * r + 3])), "l"(w23));
   }
-}
-
-// Reduce-scatter over the quad of threads that hold the same 4 keys
-// t/4 + {0, 8, 16, 24} (partials p0..p3 over different heads): keep keys
-// {c&2, (c&2)+1}, then key c.  Thread t ends with the full sum of key t/4 + 8c.
-__device__ __forceinline__ float quad_reduce(float p0, float p1, float p2, float p3, int c) {
-  const bool hi = (c & 2) != 0;
-  float k0 = hi ? p2 : p0, k1 = hi ? p3 : p1;
-  const float s0 = hi ? p0 : p2, s1 = hi ? p1 : p3;
-  k0 = __fadd_rn(k0, __shfl_xor_sync(0xFFFFFFFFu, s0, 2));
-  k1 = __fadd_rn(k1, __shfl_xor_sync(0xFFFFFFFFu, s1, 2));
-  const bool odd = (c & 1) != 0;
-  const float keep = odd ? k1 : k0;
-  const float send = odd ? k0 : k1;
-  return __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1));
 }
 
 // Threshold refresh by one warp (Methodology step 2, "Threshold Refresh"):
@@ -276,13 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = max(0, min(per_split, block_tiles - tile_lo));
 
   // ---- setup: weights, per-query state, histogram, barriers, TMEM
-  // Weights in the epilogue's order: entry [ql][c][2r + i] holds head
-  // 8r + 2c + i, so quad thread c reads its 16 weights as 4 float4 loads.
+  // Weights [ql][h] in head order (the epilogue reads 4 heads per float4
+  // broadcast).
   for (int i = tid; i < kTcQPB * kTcHeads; i += kThreads) {
     const int ql = i / kTcHeads;
-    const int c = (i % kTcHeads) / 16;
-    const int r = (i % 16) / 2;
-    const int h = 8 * r + 2 * c + (i & 1);
+    const int h = i % kTcHeads;
     float wv = 0.f;
     if (ql < nq) {
       wv = p.w[static_cast<size_t>(t0 + ql) * kTcHeads + h];
@@ -458,22 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lq = warp & 3;               // TMEM lane quarter this warp may access
       const int qh = e >> 2;                 // this warp's query within each half
       constexpr int my_halves = n_halves;
-      const int c = lane & 3;
-      const int row = lq * 32 + (lane >> 2) + 8 * c;   // key row this thread finishes
+      const int row = lq * 32 + lane;        // key row of this thread (32x32b loads)
       const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
-      // weight pairs of this thread's heads {8r + 2c, 8r + 2c + 1}, query qh of each half
-      unsigned long long wr[2][8];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const ulonglong2* src =
-            reinterpret_cast<const ulonglong2*>(w_s + (j * 4 + qh) * kTcHeads + c * 16);
-#pragma unroll
-        for (int v2 = 0; v2 < 4; ++v2) {
-          const ulonglong2 x = src[v2];
-          wr[j][2 * v2] = x.x;
-          wr[j][2 * v2 + 1] = x.y;
-        }
-      }
       // per-warp constants for the two queries (one per half)
       const int rows_i = static_cast<int>(p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF);
       int last_key[2];
@@ -520,28 +489,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           // lower bound), so the load's latency overlaps the TMEM loads
           int th_pre = 0;
           if constexpr (MODE == kModeFilter) th_pre = *reinterpret_cast<volatile int*>(&ctrl->theta[j * 4 + qh]);
-          // read the query's 64 columns of the warp's 32 lanes in four 16-lane x
-          // 32-column pieces, each load in flight while the previous piece is
-          // summed; the TMEM half goes back as soon as the last piece has landed
+          // the query's 64 head columns of this thread's key row in four 32x32b
+          // x16 loads, one in flight while the previous is summed; weights are
+          // shared-memory broadcasts
           const uint32_t ta = tq0 + acc * kN;
-          float c0[16], c1[16], c2[16], c3[16];
-          unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;   // (+0.f, +0.f)
-          tmem_ld16x256b_x4(ta, c0);
-          tmem_wait_ld_tied(c0);
-          tmem_ld16x256b_x4(ta + 32u, c1);
-          head_partials(a0, a1, c0, wr[j], 0);
-          tmem_wait_ld_tied(c1);
-          tmem_ld16x256b_x4(ta + (16u << 16), c2);
-          head_partials(a0, a1, c1, wr[j], 4);
-          tmem_wait_ld_tied(c2);
-          tmem_ld16x256b_x4(ta + (16u << 16) + 32u, c3);
-          head_partials(b0, b1, c2, wr[j], 0);
-          tmem_wait_ld_tied(c3);
+          const float4* wq = reinterpret_cast<const float4*>(w_s + (j * 4 + qh) * kTcHeads);
+          float xa[16], xb[16];
+          unsigned long long a0 = 0ull, a1 = 0ull;   // (+0.f, +0.f)
+          tmem_ld32x16(ta, xa);
+          tmem_wait_ld_tied(xa);
+          tmem_ld32x16(ta + 16u, xb);
+          head_sum16(a0, a1, xa, wq);
+          tmem_wait_ld_tied(xb);
+          tmem_ld32x16(ta + 32u, xa);
+          head_sum16(a0, a1, xb, wq + 4);
+          tmem_wait_ld_tied(xa);
+          tmem_ld32x16(ta + 48u, xb);
+          head_sum16(a0, a1, xa, wq + 8);
+          tmem_wait_ld_tied(xb);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty0 + 8 * acc);
-          head_partials(b0, b1, c3, wr[j], 4);
-          float I = quad_reduce(fold_pair(a0), fold_pair(a1), fold_pair(b0), fold_pair(b1), c);
+          head_sum16(a0, a1, xb, wq + 12);
+          float I = __fadd_rn(fold_pair(a0), fold_pair(a1));
           const int ql = j * 4 + qh;            // query within the CTA
           if constexpr (FP8) I = __fmul_rn(I, kscale);
           if constexpr (MODE == kModeDense) {

@@ -243,22 +243,6 @@ __device__ __forceinline__ void tmem_ld32x16(uint32_t taddr, float (&v)[16]) {
       : "r"(taddr));
 }
 
-// tcgen05.ld 16x256b, 4 repetitions along columns (32 fp32 columns of 16
-// lanes).  Fragment layout (PTX ISA, tcgen05 matrix fragments, shape
-// 16x256b): in repetition r, thread t holds columns 8r + 2(t%4) + {0,1} of lane
-// t/4 in registers 4r+{0,1} and of lane t/4 + 8 in registers 4r+{2,3}.
-// The registers are undefined until a tcgen05.wait::ld: read them only after
-// tmem_wait_ld_tied on the same array.
-__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, float (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
-      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
-        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
-        "=f"(v[14]), "=f"(v[15])
-      : "r"(taddr));
-}
-
 // tcgen05.wait::ld that also names the loaded registers as operands, so the
 // compiler cannot move a use of them above the wait.
 __device__ __forceinline__ void tmem_wait_ld_tied(float (&v)[16]) {
@@ -268,26 +252,6 @@ __device__ __forceinline__ void tmem_wait_ld_tied(float (&v)[16]) {
                  "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15])
                :
                : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld_tied(float (&v)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
-                 "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]),
-                 "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]),
-                 "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]),
-                 "+f"(v[24]), "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]),
-                 "+f"(v[30]), "+f"(v[31])
-               :
-               : "memory");
-}
-
-// Packed fp32x2 fused multiply-add on a bit-packed accumulator pair:
-// acc = (a0, a1) * wpair + acc, lane-wise (sm_100+).
-__device__ __forceinline__ void ffma2_acc(unsigned long long& acc, float a0, float a1,
-                                          unsigned long long wpair) {
-  unsigned long long A;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(A), "l"(wpair));
 }
 
 // Shared-memory matrix descriptor of a K-major operand stored in the
