@@ -61,7 +61,7 @@ struct Shape {
 };
 
 constexpr int kEpiWarp0 = 3;
-constexpr int kEpiWarps = 16;           // 4 per TMEM lane quarter, one query per half each
+constexpr int kEpiWarps = 16;           // 2 groups x 4 TMEM lane quarters x 2 query pairs
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kRefreshWarp = 2;
 constexpr int kN = 256;                 // MMA N: 4 queries x 64 heads
@@ -236,7 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hq0 = ALT ? nq : 4;
   constexpr int hq1 = ALT ? 0 : 4;
   constexpr int n_halves = ALT ? 1 : 2;
-  const int n_act = 4 * hq0;   // epilogue warps with work (a query in group 0)
+  const int q_acc = hq0;                                  // queries in one accumulator
+  const int warps_per_acc = 4 * (q_acc > 2 ? 2 : 1);      // epilogue warps draining one
+  const int n_act = (ALT ? 1 : 2) * warps_per_acc;        // epilogue warp-tiles per key tile
   // The key ring: kStages stages after the query rows, plus, when query group 1
   // is unused, kExtraStages more in its rows (a deeper ring for the
   // cache-streaming small-T case).
@@ -295,9 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->k_empty[s]), 1);
     }
     for (int j = 0; j < 2; ++j) {
-      const int hq = (j == 0 || alt) ? hq0 : hq1;
       mbar_init(smem_u32(&ctrl->acc_full[j]), 1);
-      mbar_init(smem_u32(&ctrl->acc_empty[j]), hq > 0 ? 4 * hq : 1);
+      mbar_init(smem_u32(&ctrl->acc_empty[j]), warps_per_acc);
     }
     mbar_init(smem_u32(&ctrl->mma_done), 1);
     mbar_fence_init();
@@ -435,113 +436,141 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    } else if (warp >= kEpiWarp0 && (warp - kEpiWarp0) / 4 < hq0) {
+    } else if (warp >= kEpiWarp0) {
       // ---------------- epilogue ----------------
+      // Two groups of 8 warps, group g draining accumulator g (so the groups
+      // run half a tile apart and one group's bin / gate / append tail
+      // overlaps the other's head sums on every scheduler); each warp covers
+      // one TMEM lane quarter and a pair of the accumulator's queries, drained
+      // back to back.
       const int e = warp - kEpiWarp0;
       const int lq = warp & 3;               // TMEM lane quarter this warp may access
-      const int qh = e >> 2;                 // this warp's query within each half
-      constexpr int my_halves = n_halves;
-      const int row = lq * 32 + lane;        // key row of this thread (32x32b loads)
-      const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
-      // per-warp constants for the two queries (one per half)
-      const int rows_i = static_cast<int>(p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF);
-      int last_key[2];
-      float qs_min[2], qdelta[2];
-      int* qhist[2];
-      unsigned long long* qcand[2];
+      const int g = e >> 3;                  // accumulator this warp drains
+      const int m = (e >> 2) & 1;            // query pair within the accumulator
+      const int nu = max(0, min(2, q_acc - 2 * m));   // queries this warp drains per tile
+      if (nu > 0) {
+        const int row = lq * 32 + lane;        // key row of this thread (32x32b loads)
+        const uint32_t lane_base = static_cast<uint32_t>(lq * 32) << 16;
+        const int qbase = (alt ? 0 : 4 * g) + 2 * m;   // first of the pair, within the CTA
+        const int rows_i = static_cast<int>(p.rows < 0x7FFFFFFF ? p.rows : 0x7FFFFFFF);
+        int last_key[2];
+        float qs_min[2], qdelta[2];
+        int* qhist[2];
+        unsigned long long* qcand[2];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int ql = j * 4 + qh;
-        const bool valid = ql < nq;
-        // a key is visible iff key <= last_key (causal position and cache end)
-        last_key[j] = valid ? min(p.causal ? ctrl->pos[ql] : 0x7FFFFFFF, rows_i - 1) : -1;
-        if constexpr (MODE == kModeFilter) {
-          qs_min[j] = ctrl->s_min[ql];
-          qdelta[j] = ctrl->delta[ql];
-          qhist[j] = hist + ql * p.nb;
-          qcand[j] = p.cand + static_cast<size_t>(valid ? t0 + ql : 0) * p.cap;
-        }
-      }
-      const uint32_t acc_full0 = smem_u32(&ctrl->acc_full[0]);
-      const uint32_t acc_empty0 = smem_u32(&ctrl->acc_empty[0]);
-      const uint32_t tq0 = tmem + lane_base + qh * kTcHeads;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int key = (tile_lo + i) * kTile + row;
-        const bool key_ok = key < rows_i;
-        float kscale = 1.f;
-        if constexpr (FP8) kscale = key_ok ? p.k_scale[key] : 0.f;
-        int kid = key;
-        if (MODE == kModeDense && p.key_ids != nullptr) kid = key_ok ? p.key_ids[key] : INT_MAX;
-        bool stop = false;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {   // query group j of the block
-          if (j >= my_halves) break;
-          const int acc = alt ? (i & 1) : j;   // accumulator holding it
-          const int use = alt ? (i >> 1) : i;
-          bool ok = mbar_wait(acc_full0 + 8 * acc, use & 1, abort_flag, p.status);
-          ok = __all_sync(0xFFFFFFFFu, ok);
-          if (!ok) {
-            stop = true;
-            break;
+        for (int u = 0; u < 2; ++u) {
+          const int ql = qbase + u;
+          const bool valid = u < nu && ql < nq;
+          // a key is visible iff key <= last_key (causal position and cache end)
+          last_key[u] = valid ? min(p.causal ? ctrl->pos[ql] : 0x7FFFFFFF, rows_i - 1) : -1;
+          if constexpr (MODE == kModeFilter) {
+            qs_min[u] = ctrl->s_min[ql];
+            qdelta[u] = ctrl->delta[ql];
+            qhist[u] = hist + ql * p.nb;
+            qcand[u] = p.cand + static_cast<size_t>(valid ? t0 + ql : 0) * p.cap;
           }
+        }
+        const uint32_t acc_full_g = smem_u32(&ctrl->acc_full[g]);
+        const uint32_t acc_empty_g = smem_u32(&ctrl->acc_empty[g]);
+        // columns of the pair in accumulator g (query 2m of the group at 64 * 2m)
+        const uint32_t ta = tmem + lane_base + static_cast<uint32_t>(g * kN + 2 * m * kTcHeads);
+        const float4* w0 = reinterpret_cast<const float4*>(w_s + qbase * kTcHeads);
+        const float4* w1 = w0 + kTcHeads / 4;
+        // ALT form: the accumulators alternate between tiles, so group g takes
+        // the tiles of parity g
+        for (int i = alt ? g : 0; i < n_tiles; i += alt ? 2 : 1) {
+          const int use = alt ? (i >> 1) : i;   // earlier tiles that used accumulator g
+          const int key = (tile_lo + i) * kTile + row;
+          const bool key_ok = key < rows_i;
+          float kscale = 1.f;
+          if constexpr (FP8) kscale = key_ok ? p.k_scale[key] : 0.f;
+          int kid = key;
+          if (MODE == kModeDense && p.key_ids != nullptr) kid = key_ok ? p.key_ids[key] : INT_MAX;
+          bool ok = mbar_wait(acc_full_g, use & 1, abort_flag, p.status);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) break;
           tc_fence_after();
-          // the threshold is read before the scores (any value read is a valid
-          // lower bound), so the load's latency overlaps the TMEM loads
-          int th_pre = 0;
-          if constexpr (MODE == kModeFilter) th_pre = *reinterpret_cast<volatile int*>(&ctrl->theta[j * 4 + qh]);
-          // the query's 64 head columns of this thread's key row in four 32x32b
-          // x16 loads, one in flight while the previous is summed; weights are
-          // shared-memory broadcasts
-          const uint32_t ta = tq0 + acc * kN;
-          const float4* wq = reinterpret_cast<const float4*>(w_s + (j * 4 + qh) * kTcHeads);
+          // the thresholds are read before the scores (any value read is a
+          // valid lower bound), so the loads' latency overlaps the TMEM loads
+          int th_pre[2] = {0, 0};
+          if constexpr (MODE == kModeFilter) {
+            th_pre[0] = *reinterpret_cast<volatile int*>(&ctrl->theta[qbase]);
+            th_pre[1] = *reinterpret_cast<volatile int*>(&ctrl->theta[qbase + 1]);
+          }
+          // each query's 64 head columns of this thread's key row in four
+          // 32x32b x16 loads, one in flight while the previous is summed; the
+          // accumulator goes back once the last load has landed
           float xa[16], xb[16];
-          unsigned long long a0 = 0ull, a1 = 0ull;   // (+0.f, +0.f)
+          unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;   // (+0.f, +0.f)
           tmem_ld32x16(ta, xa);
           tmem_wait_ld_tied(xa);
           tmem_ld32x16(ta + 16u, xb);
-          head_sum16(a0, a1, xa, wq);
+          head_sum16(a0, a1, xa, w0);
           tmem_wait_ld_tied(xb);
           tmem_ld32x16(ta + 32u, xa);
-          head_sum16(a0, a1, xb, wq + 4);
+          head_sum16(a0, a1, xb, w0 + 4);
           tmem_wait_ld_tied(xa);
           tmem_ld32x16(ta + 48u, xb);
-          head_sum16(a0, a1, xa, wq + 8);
+          head_sum16(a0, a1, xa, w0 + 8);
           tmem_wait_ld_tied(xb);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty0 + 8 * acc);
-          head_sum16(a0, a1, xb, wq + 12);
-          float I = __fadd_rn(fold_pair(a0), fold_pair(a1));
-          const int ql = j * 4 + qh;            // query within the CTA
-          if constexpr (FP8) I = __fmul_rn(I, kscale);
-          if constexpr (MODE == kModeDense) {
-            if (ql < nq && key_ok) {
-              bool vis = kid != INT_MAX;
-              if (p.causal && p.positions != nullptr) vis = vis && kid <= ctrl->pos[ql];
-              p.dense[static_cast<size_t>(t0 + ql) * p.ld + key] = vis ? I : -INFINITY;
-            }
+          if (nu == 2) {
+            tmem_ld32x16(ta + 64u, xa);
+            head_sum16(a0, a1, xb, w0 + 12);
+            tmem_wait_ld_tied(xa);
+            tmem_ld32x16(ta + 80u, xb);
+            head_sum16(b0, b1, xa, w1);
+            tmem_wait_ld_tied(xb);
+            tmem_ld32x16(ta + 96u, xa);
+            head_sum16(b0, b1, xb, w1 + 4);
+            tmem_wait_ld_tied(xa);
+            tmem_ld32x16(ta + 112u, xb);
+            head_sum16(b0, b1, xa, w1 + 8);
+            tmem_wait_ld_tied(xb);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty_g);
+            head_sum16(b0, b1, xb, w1 + 12);
           } else {
-            const int b = bin_of(I, qs_min[j], qdelta[j], p.nb);
-            const int th = th_pre;
-            const bool pass = key <= last_key[j] && b >= th;
-            const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
-            if (m != 0) {
-              const int leader = __ffs(m) - 1;
-              int base = 0;
-              if (lane == leader)
-                base = shared_query ? atomicAdd(&p.cnt[t0 + ql], __popc(m))
-                                    : atomicAdd(&ctrl->cnt[ql], __popc(m));
-              base = __shfl_sync(0xFFFFFFFFu, base, leader);
-              if (pass) {
-                const int slot = base + __popc(m & ((1u << lane) - 1u));
-                if (slot < p.cap) qcand[j][slot] = cand_pack(I, key);
-                atomicAdd(&qhist[j][b], 1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty_g);
+            head_sum16(a0, a1, xb, w0 + 12);
+          }
+          const float I_pair[2] = {__fadd_rn(fold_pair(a0), fold_pair(a1)),
+                                   __fadd_rn(fold_pair(b0), fold_pair(b1))};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (u >= nu) break;
+            const int ql = qbase + u;   // query within the CTA
+            float I = I_pair[u];
+            if constexpr (FP8) I = __fmul_rn(I, kscale);
+            if constexpr (MODE == kModeDense) {
+              if (ql < nq && key_ok) {
+                bool vis = kid != INT_MAX;
+                if (p.causal && p.positions != nullptr) vis = vis && kid <= ctrl->pos[ql];
+                p.dense[static_cast<size_t>(t0 + ql) * p.ld + key] = vis ? I : -INFINITY;
+              }
+            } else {
+              const int b = bin_of(I, qs_min[u], qdelta[u], p.nb);
+              const bool pass = key <= last_key[u] && b >= th_pre[u];
+              const unsigned msk = __ballot_sync(0xFFFFFFFFu, pass);
+              if (msk != 0) {
+                const int leader = __ffs(msk) - 1;
+                int base = 0;
+                if (lane == leader)
+                  base = shared_query ? atomicAdd(&p.cnt[t0 + ql], __popc(msk))
+                                      : atomicAdd(&ctrl->cnt[ql], __popc(msk));
+                base = __shfl_sync(0xFFFFFFFFu, base, leader);
+                if (pass) {
+                  const int slot = base + __popc(msk & ((1u << lane) - 1u));
+                  if (slot < p.cap) qcand[u][slot] = cand_pack(I, key);
+                  atomicAdd(&qhist[u][b], 1);
+                }
               }
             }
           }
+          if (lane == 0) atomicAdd(&ctrl->tiles_done, 1);
         }
-        if (stop) break;
-        if (lane == 0) atomicAdd(&ctrl->tiles_done, 1);
       }
     }
   }
