@@ -31,6 +31,12 @@
 //     threshold refresh.
 //   * Work units: whole query blocks, or key ranges of a query block split
 //     over several CTAs (they share the query's count and a global histogram).
+//   * Scan order (general form, filter mode): a CTA starts at the filter's
+//     current sweep position (tiles scanned by all CTAs / SMs, mod its range)
+//     and wraps around, so CTAs that start in later waves read the key tiles
+//     the running CTAs read, while L2 still holds them (1M bf16: 3.3 instead
+//     of 9.0 GB of DRAM reads per launch).  The result does not depend on the
+//     order: every visible key is scored once and the threshold only rises.
 //   * ALT form (T <= 4): one query group with a narrower MMA (N = 64 per
 //     query), the two accumulators alternating between tiles, and the unused
 //     query rows used as two more key stages.
@@ -77,7 +83,7 @@ struct __align__(8) Ctrl {
   uint32_t tmem_base;
   int abort_flag;
   int tiles_done;                        // epilogue warp-tiles finished
-  int pad0;
+  int rot;                               // first tile of the scan, relative to tile_lo
   float s_min[kTcQPB];
   float delta[kTcQPB];
   int theta[kTcQPB];
@@ -291,6 +297,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     ctrl->abort_flag = 0;
     ctrl->tiles_done = 0;
+    // the scan starts at the filter's current sweep position (when it falls in
+    // this unit's range) and wraps around; any order gives the same result
+    int rot = 0;
+    if (MODE == kModeFilter && !ALT && p.sweep != nullptr && n_tiles > 1) {
+      const unsigned long long done = *reinterpret_cast<volatile unsigned long long*>(p.sweep);
+      const long long pos = static_cast<long long>(done / static_cast<unsigned long long>(p.num_sms)) %
+                            block_tiles;
+      const long long rel = pos - tile_lo;
+      if (rel > 0 && rel < n_tiles) rot = static_cast<int>(rel);
+    }
+    ctrl->rot = rot;
     mbar_init(smem_u32(&ctrl->q_full), 1);
     for (int s = 0; s < Sh::kMaxStages; ++s) {
       mbar_init(smem_u32(&ctrl->k_full[s]), 1);
@@ -308,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
+  const int rot = ctrl->rot;
 
   if (n_tiles > 0) {
     if (warp == 0) {
@@ -332,8 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&ctrl->k_full[s]);
           mbar_arrive_expect_tx(fb, Sh::kKStage);
           const uint32_t dst = k_stage(s);
+          const int ti = i + rot < n_tiles ? i + rot : i + rot - n_tiles;   // rotated scan
           for (int c = 0; c < Sh::kChunks; ++c)
-            tma_load_2d(dst + c * Sh::kKChunkBytes, &k_map, c * Sh::kBoxCols, (tile_lo + i) * kTile, fb);
+            tma_load_2d(dst + c * Sh::kKChunkBytes, &k_map, c * Sh::kBoxCols, (tile_lo + ti) * kTile, fb);
           issued[s] = i;
         }
         if (*abort_flag) {
@@ -399,6 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ab = __shfl_sync(0xFFFFFFFFu, *abort_flag, 0);
             if (done >= n_tiles || ab) break;
             if (done != prev_done) {
+              // advance the filter's sweep counter in steps of 16 tiles (the
+              // start of a later CTA's scan; off the MMA and copy paths)
+              if (lane == 0 && p.sweep != nullptr && prev_done >= 0 && (done >> 4) > (prev_done >> 4))
+                atomicAdd(p.sweep, static_cast<unsigned long long>(16 * ((done >> 4) - (prev_done >> 4))));
               prev_done = done;
               t_prog = globaltimer_ns();
             }
@@ -480,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the tiles of parity g
         for (int i = alt ? g : 0; i < n_tiles; i += alt ? 2 : 1) {
           const int use = alt ? (i >> 1) : i;   // earlier tiles that used accumulator g
-          const int key = (tile_lo + i) * kTile + row;
+          const int ti = i + rot < n_tiles ? i + rot : i + rot - n_tiles;   // rotated scan
+          const int key = (tile_lo + ti) * kTile + row;
           const bool key_ok = key < rows_i;
           float kscale = 1.f;
           if constexpr (FP8) kscale = key_ok ? p.k_scale[key] : 0.f;

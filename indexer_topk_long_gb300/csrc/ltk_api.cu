@@ -63,7 +63,8 @@ struct ltk_handle {
   int timing = 0;
   int ring_calls = 0;                  // timed calls since timing was enabled
   cudaEvent_t* ev = nullptr;           // events of the current call (or null)
-  unsigned long long* pairs = nullptr; // [1] visible pairs of the last call
+  unsigned long long* pairs = nullptr; // [2] visible pairs of the last call; key tiles scanned so
+                                       // far by the filter (its sweep position, see ScoreParams)
   int last_kind = 0;                   // 0 none, 1 fused, 2 decoupled
   // last call
   int last_T = 0;
@@ -443,7 +444,7 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   h->ev = begin_timed_call(h);
   if (h->ev) LTK_CUDA(cudaEventRecord(h->ev[0], st));
   LTK_CUDA(cudaMemsetAsync(h->status, 0, sizeof(int), st));
-  LTK_CUDA(cudaMemsetAsync(h->pairs, 0, sizeof(unsigned long long), st));
+  LTK_CUDA(cudaMemsetAsync(h->pairs, 0, 2 * sizeof(unsigned long long), st));
   LTK_CUDA(cudaMemsetAsync(h->ovf, 0, 2 * sizeof(int), st));
 
   // ---- Sample (Methodology step 1)
@@ -515,6 +516,8 @@ ltk_status run_fused(ltk_handle* h, const CallArgs& a, const int* prev_topk, int
   fp.k = a.k;
   fp.refresh_interval = c.refresh_interval;
   fp.skip_key_loads = (c.debug_flags & 1) ? 1 : 0;
+  fp.sweep = h->pairs + 1;
+  fp.num_sms = h->num_sms;
   fp.ghist = h->ghist;
   fp.status = h->status;
   plan_work(h, a.T, a.S, false, &fp.b_full, &fp.s_last, &qpu);
@@ -683,7 +686,7 @@ ltk_status ltk_create(const ltk_config* cfg, ltk_handle** out) {
     step(alloc(&h->io_oidx, T * cfg->k * 4ull));
     step(alloc(&h->io_oscore, T * cfg->k * 4ull));
   }
-  step(alloc(&h->pairs, 8));
+  step(alloc(&h->pairs, 16));
   for (auto& row : h->ring)
     for (auto& ev : row) step(cudaEventCreate(&ev));
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, 4);

@@ -337,6 +337,13 @@ struct ScoreParams {
   int b_full;
   int s_last;
   int* ghist;
+  // Filter sweep (indexer scorer, general form; null: every CTA scans its key
+  // range from the first tile): key tiles scanned so far by all CTAs, zeroed
+  // before the launch.  A CTA starts its range at tile (sweep / num_sms) mod
+  // its block's tiles and wraps around, so CTAs that start in later waves
+  // read the tiles the running ones are reading, while L2 still holds them.
+  unsigned long long* sweep;
+  int num_sms;
   // Segmented lists (retrieval scorer): query t's list holds nseg segments of
   // seg_cap entries, segment s written only by the CTA scanning range s with
   // a CTA-local count; seg_cnt [T, nseg] receives the counts, and cnt[t] is
