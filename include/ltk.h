@@ -52,7 +52,7 @@ typedef enum {
   LTK_ERR_OVERFLOW = 4,     /* informational: candidate list overflowed; the
                                affected queries were recomputed exactly      */
   LTK_ERR_TIMEOUT = 5,      /* a bounded device-side wait expired             */
-  LTK_ERR_UNSUPPORTED = 6   /* shape or mode this build does not implement    */
+  LTK_ERR_UNSUPPORTED = 6   /* shape or mode the library does not implement   */
 } ltk_status;
 
 typedef enum { LTK_BF16 = 0, LTK_FP8_E4M3 = 1 } ltk_dtype;
