@@ -114,6 +114,28 @@ def test_result_independent_of_sample_bins_and_refresh():
     check_tolerant(inp, outs[0][0].cpu().numpy(), outs[0][1].cpu().numpy(), 1024)
 
 
+def test_scan_order_does_not_change_results():
+    """More query blocks than SMs, so CTAs of later waves start their key scan
+    at the filter's sweep position and wrap around; with refresh_interval=0 the
+    sweep counter never advances and every CTA scans from the first tile.  Both
+    orders (and a sparser refresh) must give the same bits, and the oracle's."""
+    import torch
+    T, S = 2432, 40000          # 304 query blocks: two waves of 152
+    inp = datagen.make_indexer_inputs(T=T, first_pos=S - T, S=S, integer=True, seed=21)
+    d = to_device(inp)
+    outs = []
+    for cfg in (dict(refresh_interval=0), dict(), dict(refresh_interval=7)):
+        op = IndexerTopK(max_T=T, max_S=S, k=512, **cfg)
+        outs.append(op(d["q"], d["w"], d["k_cache"], d["positions"], k=512))
+        torch.cuda.synchronize()
+        assert op.stats()["device_status"] == 0
+        op.close()
+    for i, (a, b) in enumerate(outs[1:]):
+        assert torch.equal(a, outs[0][0]) and torch.equal(b, outs[0][1]), f"variant {i + 1}"
+    qs = [0, 1, 607, 1215, 1823, 2400, T - 2, T - 1]
+    check_exact(inp, outs[1][0].cpu().numpy(), outs[1][1].cpu().numpy(), 512, queries=qs)
+
+
 def test_overflow_is_rescued_exactly():
     inp = datagen.make_indexer_inputs(T=12, first_pos=3000, S=3100, integer=True, seed=10)
     idx, sc, st = _run(inp, 300, cand_cap=320, refresh_interval=0, n_bins=32)
