@@ -17,16 +17,18 @@
 //     (one query group, half of the block): keys sit on TMEM lanes.  TMEM (512
 //     columns) holds two accumulators, one per group; the epilogue drains one
 //     while the tensor core fills the other.
-//   * Epilogue (16 warps, one per TMEM lane quarter and query of a group):
-//     one thread per key row.  The query's 64 head columns of the thread's
-//     row come in four tcgen05.ld 32x32b.x16 pieces (the TMEM read shape with
-//     the highest bandwidth), each in flight while the previous one is summed,
-//     and the accumulator goes back once the last piece has landed; ReLU
-//     (x + |x| as a packed fp32x2 add) and the w-weighted head sum (packed
-//     fp32x2 FMAs, weights as shared-memory broadcasts) run two heads per
-//     instruction, and each thread ends with its key's whole score -> mask ->
-//     [dense: store I] or [filter: bin, gate, warp ballot append,
-//     shared-memory histogram].
+//   * Epilogue (16 warps in two groups of 8, group g draining accumulator g
+//     only, so the two groups run apart and one group's gate / append tail
+//     overlaps the other's head sums): one thread per key row, each warp one
+//     TMEM lane quarter and two of the group's queries.  A query's 64 head
+//     columns of the thread's row come in four tcgen05.ld 32x32b.x16 pieces
+//     (the TMEM read shape with the highest bandwidth), the warp's eight pieces
+//     each in flight while the previous one is summed, and the accumulator
+//     goes back once the last piece has landed; ReLU (x + |x| as a packed
+//     fp32x2 add) and the w-weighted head sum (packed fp32x2 FMAs, weights as
+//     shared-memory broadcasts) run two heads per instruction, and each thread
+//     ends with its key's whole score -> mask -> [dense: store I] or [filter:
+//     bin, gate, warp ballot append, shared-memory histogram].
 //   * Warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer, warp 2 =
 //     threshold refresh.
 //   * Work units: whole query blocks, or key ranges of a query block split
@@ -34,8 +36,8 @@
 //   * Scan order (general form, filter mode): a CTA starts at the filter's
 //     current sweep position (tiles scanned by all CTAs / SMs, mod its range)
 //     and wraps around, so CTAs that start in later waves read the key tiles
-//     the running CTAs read, while L2 still holds them (1M bf16: 3.3 instead
-//     of 9.0 GB of DRAM reads per launch).  The result does not depend on the
+//     the running CTAs read, while L2 still holds them (1M bf16: 3.3-5.5
+//     instead of 9.0 GB of DRAM reads per launch).  The result does not depend on the
 //     order: every visible key is scored once and the threshold only rises.
 //   * ALT form (T <= 4): one query group with a narrower MMA (N = 64 per
 //     query), the two accumulators alternating between tiles, and the unused
