@@ -78,3 +78,29 @@ def test_fp8_overflow_rescue():
     idx, sc, _, _, st = _fused_and_decoupled(inp, k, cand_cap=1024, refresh_interval=0, n_bins=32)
     assert st["n_overflow"] > 0
     check_tolerant(inp, idx, sc, k)
+
+
+def _fp8_integer_inputs(T, S, seed):
+    """e4m3 codes of small integers (-3..3 are exact in e4m3) with per-token
+    power-of-two scales and power-of-two weights: every product and partial
+    sum is exact in fp32, so the kernel must return the oracle's result bit
+    for bit."""
+    import oracle.indexer_topk as orc
+    base = datagen.make_indexer_inputs(T=T, first_pos=S - T, S=S, integer=True, seed=seed)
+    q8 = datagen.e4m3_codes(orc.bf16_to_f64(base.q)).reshape(base.q.shape)
+    k8 = datagen.e4m3_codes(orc.bf16_to_f64(base.k)).reshape(base.k.shape)
+    qs = np.ldexp(np.ones(T, np.float32), -(np.arange(T) % 3)).astype(np.float32)
+    ks = np.ldexp(np.ones(S, np.float32), (np.arange(S) % 5) - 2).astype(np.float32)
+    return datagen.IndexerInputs("fp8", q8, k8, base.w, base.positions, qs, ks)
+
+
+@pytest.mark.parametrize("T,S,k", [(37, 30001, 1000), (1300, 20000, 512)])
+def test_fp8_integer_codes_exact(T, S, k):
+    from parity import check_exact
+    inp = _fp8_integer_inputs(T, S, seed=800 + T)
+    idx, sc, di, ds, st = _fused_and_decoupled(inp, k)
+    assert st["n_overflow"] == 0
+    rows = None if T < 100 else sorted({0, 1, 7, 8, 640, 647, T - 2, T - 1})
+    check_exact(inp, idx, sc, k, queries=rows)
+    np.testing.assert_array_equal(di, idx)
+    np.testing.assert_array_equal(ds, sc)
