@@ -94,7 +94,8 @@ def _fp8_integer_inputs(T, S, seed):
     return datagen.IndexerInputs("fp8", q8, k8, base.w, base.positions, qs, ks)
 
 
-@pytest.mark.parametrize("T,S,k", [(37, 30001, 1000), (1300, 20000, 512)])
+@pytest.mark.parametrize("T,S,k", [(1, 300000, 2048), (3, 9001, 256), (4, 20000, 300),
+                                   (37, 30001, 1000), (1300, 20000, 512)])
 def test_fp8_integer_codes_exact(T, S, k):
     from parity import check_exact
     inp = _fp8_integer_inputs(T, S, seed=800 + T)
