@@ -602,7 +602,8 @@ def decode_record(T: int, dtype: str, engine: str, steps: int, warmup: int, dev,
                                    f"d=128, k=2048, previous-step sample; keys split over the GPU",
                        "engine": engine},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak,
+                         "traffic": recorded_traffic(f"score_filter_decode_t{T}_{dtype}") if engine == "auto" else None,
                          "kernel": "filter stage (score_tc_kernel<filter>, keys split over the GPU)",
                          "peak_source": f"{kind} " + ("copy bandwidth" if bound == "hbm" else "bf16 sustained"),
                          "algorithmic_bytes_per_call": k_bytes, "algorithmic_flop_per_call": flop},
